@@ -1,0 +1,217 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 linear-layer engine.
+ *
+ * The engine implements the NVFP4 recipe of "Pretraining Large Language
+ * Models with NVFP4" (arXiv 2509.25149; summary page, format paragraph,
+ * recipe paragraph and limitations paragraph) and of the NVIDIA blog post
+ * "NVFP4 Trains with Precision of 16-Bit and Speed and Efficiency of 4-Bit"
+ * (technique list):
+ *   - a full-tensor amax sets an FP32 tensor scale (S_dec = A/2688,
+ *     S_enc = 2688/A, 2688 = 6 * 448);
+ *   - 16 consecutive elements share one E4M3 block scale (1x16 blocks for
+ *     activations and gradients; one scale per 16x16 tile for weights);
+ *   - elements are E2M1 codes {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6},
+ *     two per byte, rounded to nearest-even or stochastically (Philox);
+ *   - Wgrad inputs first get a 16-point random Hadamard transform along the
+ *     token (reduction) dimension;
+ *   - Fprop, Dgrad and Wgrad run as block-scaled FP4 GEMMs with FP32
+ *     accumulation on the tensor cores.
+ *
+ * Conventions for every entry point
+ *   - All pointers named "device" are CUDA device pointers on the current
+ *     device; the caller allocates and owns every buffer.  The library
+ *     allocates no device memory.
+ *   - Calls are asynchronous on `stream` (cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are detected on the host, return at
+ *     once and launch nothing.  Conditions found on the device (non-finite
+ *     input, a pipeline wait that ran out) are recorded in a per-device
+ *     status word that nvfp4_sync_status() reads and clears.
+ *   - Inputs are row-major.  Device pointers must be 16-byte aligned and
+ *     row strides (ldx, ld_codes, ldc) multiples of 16 bytes.
+ *   - Numerics follow this contract bit for bit (the pages leave the
+ *     formulas open; these are the plain readings): FP32 steps are
+ *     correctly rounded single operations, in this order:
+ *       A = max|x|;  S_dec = fl(A/2688);  S_enc = fl(2688/A) (FLT_MAX if it
+ *       overflows; A == 0 gives S_dec = S_enc = 1);
+ *       per block: sb = E4M3_rne_satfinite(fl(fl(bamax/6) * S_enc));
+ *       r = fl(S_enc/sb) (FLT_MAX if it overflows);  v = fl(x * r);
+ *       RTN: nearest E2M1 of clamp(|v|, 6), ties to the even mantissa, sign
+ *       kept (a negative value that rounds to 0 gives code 0x8);
+ *       SR: u = Philox4x32-10(key = seed, counter = (i/4, 0, 0, 0))[i%4] >> 8,
+ *       round |v| up iff u * 2^-24 < (|v| - lo)/(hi - lo), where i is the
+ *       element's row-major index in the logical output tensor;
+ *       sb == 0: every code of the block is 0.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* nvfp4_stream_t;
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, bad enum */
+    NVFP4_ERR_UNSUPPORTED = 2, /* valid request this build does not implement   */
+    NVFP4_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
+    NVFP4_ERR_NONFINITE = 4,   /* (device) the input held a NaN or an infinity  */
+    NVFP4_ERR_TIMEOUT = 5,     /* (device) a bounded pipeline wait ran out      */
+    NVFP4_ERR_CUDA = 6         /* a CUDA runtime call failed                    */
+} nvfp4_status;
+
+typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
+typedef enum { NVFP4_BLOCK_1x16 = 0, NVFP4_BLOCK_16x16 = 1 } nvfp4_block;
+typedef enum { NVFP4_RTN = 0, NVFP4_SR = 1 } nvfp4_round;
+
+/*
+ * Block-scale layouts.
+ *   NVFP4_SCALES_LINEAR: byte (r, kb) at r * (cols/16) + kb, where kb = c/16.
+ *     For 16x16 blocks the scale of tile (r/16, kb) is repeated on each of
+ *     the tile's 16 rows, so both layouts index scales per row.
+ *   NVFP4_SCALES_MMA: the tensor-core layout the GEMM reads.  Rows are taken
+ *     in groups of 128 and K blocks in groups of 4 ("atoms" of 512 bytes);
+ *     with n_katoms = 4 * ceil(cols/256),
+ *       byte (r, kb) = ((r/128) * n_katoms + kb/4) * 512
+ *                      + (r%32) * 16 + ((r/32)%4) * 4 + kb%4.
+ *     Padding (rows up to a multiple of 128, K blocks up to n_katoms * 4)
+ *     is written as zero by the quantize calls.
+ *   nvfp4_scales_bytes() gives the buffer size of either layout.
+ */
+typedef enum { NVFP4_SCALES_LINEAR = 0, NVFP4_SCALES_MMA = 1 } nvfp4_scale_layout;
+
+/*
+ * One quantized NVFP4 tensor: the logical [rows][cols] matrix the codes
+ * describe, blocks along cols (the GEMM's K).
+ *   codes  device, [rows][ld_codes] bytes; element c of a row in byte c/2,
+ *          even c in the low nibble.  ld_codes >= cols/2, multiple of 16.
+ *   scales device, E4M3 block scales in `scale_layout`.
+ *   amax   device float[3] = {A, S_dec, S_enc}, written by quantize calls
+ *          and read by the GEMM (alpha = S_dec(A) * S_dec(B)).
+ */
+typedef struct {
+    uint8_t* codes;
+    uint8_t* scales;
+    float* amax;
+    int64_t rows;
+    int64_t cols;
+    int64_t ld_codes;
+    int32_t scale_layout; /* nvfp4_scale_layout */
+    int32_t reserved;     /* must be 0 */
+} nvfp4_tensor;
+
+/* Bytes of the scale buffer of a [rows][cols] tensor in `scale_layout`
+ * (0 for invalid arguments). */
+size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout);
+
+/* Workspace bytes needed by the quantize, RHT-quantize and GEMM calls for
+ * any shape (the amax pass keeps one partial per CTA there). */
+size_t nvfp4_workspace_size(void);
+
+/*
+ * nvfp4_quantize -- tensor amax (one full read), then block scales and
+ * E2M1 codes (a second read), per the format paragraph of the paper page
+ * and the blog's micro-block / 2D-block / stochastic-rounding items.
+ *   x            device, [rows][ldx] elements of `dtype` (ldx >= cols).
+ *   block        1x16 (activations, gradients) or 16x16 (weights; RTN only,
+ *                rows % 16 == 0).
+ *   round, seed  rounding mode and the Philox key for SR.
+ *   out_rowwise  if non-NULL: describes x, [rows][cols], blocks along cols
+ *                (cols % 16 == 0).
+ *   out_colwise  if non-NULL: describes x^T, [cols][rows], blocks along rows
+ *                (rows % 16 == 0).  At least one output must be given; both
+ *                get the same {A, S_dec, S_enc}.
+ *   workspace    device, >= nvfp4_workspace_size() bytes, 16-byte aligned;
+ *                no initial contents needed; must not be shared by calls
+ *                that run concurrently.
+ */
+nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                            nvfp4_block block, nvfp4_round round, uint64_t seed,
+                            const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
+                            void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_rht_quantize -- the Wgrad operand path (paper page, limitations
+ * paragraph: Hadamard only on Wgrad; blog: Hadamard transforms reshape the
+ * distribution).  Every run of 16 consecutive rows (tokens) of each column
+ * is transformed y = (1/4) H16 (d . x), H16 Sylvester, d_j = +-1 from bit j
+ * of word 0 of Philox4x32-10(key = rht_seed, counter = (0, 0, 1, 0)), the
+ * butterfly evaluated stage by stage over index bits 0..3 in FP32.  Then the
+ * tensor amax of y, and y^T is quantized with 1x16 blocks along the rows.
+ *   out_colwise  describes y^T, [cols][rows]; rows % 16 == 0.
+ *   Other arguments as nvfp4_quantize.  Both Wgrad operands must use the
+ *   same rht_seed so the transform cancels in the product.
+ */
+nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                nvfp4_round round, uint64_t seed, uint64_t rht_seed,
+                                const nvfp4_tensor* out_colwise, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm -- C[m][n] = S_dec(A) S_dec(B) sum_kb sbA[m][kb] sbB[n][kb]
+ *               sum_{16} e2m1(A[m][k]) e2m1(B[n][k]),
+ * a block-scaled FP4 GEMM on the tcgen05 tensor cores with FP32
+ * accumulation (blog: Blackwell FP4 tensor cores run the linear layers).
+ *   A            [M][K] quantized, B [N][K] quantized, both NVFP4_SCALES_MMA,
+ *                A->cols == B->cols == K, K % 64 == 0.
+ *   C            device, [M][ldc] of out_dtype (bf16 or fp32), written whole.
+ *   workspace    as nvfp4_quantize (may be NULL with 0 bytes: the GEMM
+ *                needs none today).
+ */
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,
+                        int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * Linear layer Y = X W^T with NVFP4 GEMMs, following the recipe (paper
+ * page: 2D weight scaling keeps Fprop and Dgrad consistent, Hadamard only on
+ * Wgrad; blog: stochastic rounding on gradients):
+ *   fwd:  X -> xq (1x16 RTN);  W -> wq and wtq (16x16 RTN, both layouts);
+ *         Y[M][N] (bf16) = gemm(xq, wq).
+ *   bwd:  dY -> dyq (1x16 SR);  dX[M][K] (bf16) = gemm(dyq, wtq);
+ *         RHT along tokens with rht_seed, then dY^T -> dytq (SR) and
+ *         X^T -> xtq (RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
+ * The context holds caller-allocated quantized buffers; every tensor's
+ * rows/cols/ld_codes/scale_layout (MMA) must be filled in for the shapes
+ * above, and the workspace as for nvfp4_quantize.  X, W, dY are bf16,
+ * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
+ * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).
+ */
+typedef struct {
+    int64_t M, N, K;
+    nvfp4_tensor xq;   /* [M][K]  */
+    nvfp4_tensor wq;   /* [N][K]  */
+    nvfp4_tensor wtq;  /* [K][N]  */
+    nvfp4_tensor dyq;  /* [M][N]  */
+    nvfp4_tensor dytq; /* [N][M]  */
+    nvfp4_tensor xtq;  /* [K][M]  */
+    void* workspace;
+    size_t workspace_bytes;
+} nvfp4_linear_ctx;
+
+nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
+nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,
+                              uint64_t rht_seed, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
+
+/* Synchronize `stream`, then return and clear the device status word of the
+ * current device: NVFP4_ERR_NONFINITE, NVFP4_ERR_TIMEOUT or NVFP4_OK
+ * (NVFP4_ERR_CUDA if the synchronization itself failed). */
+nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream);
+
+/* Static English text of a status code. */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Text of the last error seen by this thread in a call of this library
+ * (empty if none); valid until the thread's next call. */
+const char* nvfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,0 +1,295 @@
+"""GB300 (sm_103a) NVFP4 linear-layer engine: Python binding of the C ABI.
+
+The binding only marshals arguments: every step of quantization and of the
+GEMMs runs in the CUDA library ``_build/libnvfp4_gb300.so`` (built by
+``build.py``).  PyTorch supplies device memory and the current stream.  The
+functions carry the names of the C entry points in ``include/nvfp4.h``.
+
+If the library is missing the import of the binding fails loudly; there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
+    "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "empty_qtensor", "scales_as_linear",
+]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA = range(7)
+IN_BF16, IN_FP32 = 0, 1
+OUT_BF16, OUT_FP32 = 0, 1
+BLOCK_1x16, BLOCK_16x16 = 0, 1
+RTN, SR = 0, 1
+SCALES_LINEAR, SCALES_MMA = 0, 1
+
+_BLOCKS = {"1x16": BLOCK_1x16, "16x16": BLOCK_16x16}
+_ROUNDS = {"rtn": RTN, "sr": SR}
+_LAYOUTS = {"linear": SCALES_LINEAR, "mma": SCALES_MMA}
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({detail})")
+
+
+class nvfp4_tensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("amax", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld_codes", ctypes.c_int64),
+                ("scale_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class nvfp4_linear_ctx(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("xq", nvfp4_tensor), ("wq", nvfp4_tensor), ("wtq", nvfp4_tensor), ("dyq", nvfp4_tensor),
+                ("dytq", nvfp4_tensor), ("xtq", nvfp4_tensor),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise ImportError(f"NVFP4 CUDA library not built: {_build.LIB} is missing "
+                                  "(run quantize_block_scaled_amax_gb300.build.build())")
+            L = ctypes.CDLL(_build.LIB)
+            st = ctypes.c_int
+            vp = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            u64 = ctypes.c_uint64
+            tp = ctypes.POINTER(nvfp4_tensor)
+            L.nvfp4_scales_bytes.restype = ctypes.c_size_t
+            L.nvfp4_scales_bytes.argtypes = [i64, i64, ctypes.c_int32]
+            L.nvfp4_workspace_size.restype = ctypes.c_size_t
+            L.nvfp4_workspace_size.argtypes = []
+            L.nvfp4_quantize.restype = st
+            L.nvfp4_quantize.argtypes = [vp, st, i64, i64, i64, st, st, u64, tp, tp, vp, ctypes.c_size_t, vp]
+            L.nvfp4_rht_quantize.restype = st
+            L.nvfp4_rht_quantize.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t, vp]
+            L.nvfp4_gemm.restype = st
+            L.nvfp4_gemm.argtypes = [tp, tp, vp, st, i64, vp, ctypes.c_size_t, vp]
+            L.nvfp4_linear_fwd.restype = st
+            L.nvfp4_linear_fwd.argtypes = [vp, vp, vp, ctypes.POINTER(nvfp4_linear_ctx), vp]
+            L.nvfp4_linear_bwd.restype = st
+            L.nvfp4_linear_bwd.argtypes = [vp, vp, vp, vp, u64, u64, ctypes.POINTER(nvfp4_linear_ctx), vp]
+            L.nvfp4_sync_status.restype = st
+            L.nvfp4_sync_status.argtypes = [vp]
+            L.nvfp4_status_string.restype = ctypes.c_char_p
+            L.nvfp4_status_string.argtypes = [st]
+            L.nvfp4_last_error.restype = ctypes.c_char_p
+            L.nvfp4_last_error.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        L = lib()
+        detail = (L.nvfp4_last_error() or b"").decode() or L.nvfp4_status_string(status).decode()
+        raise NVFP4Error(status, where, detail)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def nvfp4_scales_bytes(rows: int, cols: int, scale_layout: str = "mma") -> int:
+    return int(lib().nvfp4_scales_bytes(rows, cols, _LAYOUTS[scale_layout]))
+
+
+def nvfp4_workspace_size() -> int:
+    return int(lib().nvfp4_workspace_size())
+
+
+_ws: dict = {}
+
+
+def _workspace(device) -> torch.Tensor:
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    w = _ws.get(key)
+    if w is None:
+        w = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
+        _ws[key] = w
+    return w
+
+
+class QTensor:
+    """A quantized NVFP4 tensor held in torch device buffers.
+
+    codes  uint8 [rows][ld_codes] (two E2M1 codes per byte, low nibble first)
+    scales uint8 flat buffer, E4M3 block scales in ``scale_layout``
+    amax   float32 [3] = (A, S_dec, S_enc)
+    """
+
+    def __init__(self, codes, scales, amax, rows, cols, scale_layout):
+        self.codes, self.scales, self.amax = codes, scales, amax
+        self.rows, self.cols = int(rows), int(cols)
+        self.scale_layout = scale_layout
+
+    @property
+    def ld_codes(self) -> int:
+        return int(self.codes.stride(0))
+
+    def c(self) -> nvfp4_tensor:
+        return nvfp4_tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.amax.data_ptr(), self.rows,
+                            self.cols, self.ld_codes, _LAYOUTS[self.scale_layout], 0)
+
+
+def empty_qtensor(rows: int, cols: int, device, scale_layout: str = "mma") -> QTensor:
+    ld = ((cols // 2 + 15) // 16) * 16
+    codes = torch.empty(rows, ld, dtype=torch.uint8, device=device)
+    scales = torch.empty(max(nvfp4_scales_bytes(rows, cols, scale_layout), 16), dtype=torch.uint8, device=device)
+    amax = torch.empty(4, dtype=torch.float32, device=device)
+    return QTensor(codes, scales, amax, rows, cols, scale_layout)
+
+
+def _in_dtype(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return IN_BF16
+    if x.dtype == torch.float32:
+        return IN_FP32
+    raise TypeError(f"input dtype {x.dtype} not supported (bf16 or fp32)")
+
+
+def _check_input(x: torch.Tensor):
+    if not x.is_cuda:
+        raise ValueError("input must be a CUDA tensor")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("input must be a 2D row-major tensor")
+
+
+def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", seed: int = 0, *,
+                   rowwise: bool = True, colwise: bool = False, scale_layout: str = "mma",
+                   out_rowwise: QTensor | None = None, out_colwise: QTensor | None = None, stream=None):
+    """Quantize x [rows][cols]; returns (rowwise QTensor or None, colwise QTensor or None)."""
+    _check_input(x)
+    rows, cols = x.shape
+    if rowwise and out_rowwise is None:
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout)
+    if colwise and out_colwise is None:
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+    r = out_rowwise.c() if rowwise else None
+    c = out_colwise.c() if colwise else None
+    ws = _workspace(x.device)
+    st = lib().nvfp4_quantize(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _BLOCKS[block], _ROUNDS[round],
+                              seed, ctypes.byref(r) if r is not None else None,
+                              ctypes.byref(c) if c is not None else None, ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "nvfp4_quantize")
+    return (out_rowwise if rowwise else None), (out_colwise if colwise else None)
+
+
+def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,
+                       scale_layout: str = "mma", out_colwise: QTensor | None = None, stream=None) -> QTensor:
+    """16-point RHT along the rows of x, then colwise 1x16 quantization of the result's transpose."""
+    _check_input(x)
+    rows, cols = x.shape
+    if out_colwise is None:
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+    c = out_colwise.c()
+    ws = _workspace(x.device)
+    st = lib().nvfp4_rht_quantize(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
+                                  rht_seed, ctypes.byref(c), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "nvfp4_rht_quantize")
+    return out_colwise
+
+
+def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """C[M][N] = dequant(a) @ dequant(b)^T on the FP4 tensor cores (FP32 accumulation)."""
+    if out is None:
+        out = torch.empty(a.rows, b.rows, dtype=out_dtype, device=a.codes.device)
+    od = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32}[out.dtype]
+    ca, cb = a.c(), b.c()
+    st = lib().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), out.data_ptr(), od, out.stride(0), None, 0,
+                          _stream(stream))
+    _check(st, "nvfp4_gemm")
+    return out
+
+
+class LinearContext:
+    """Caller-owned quantized buffers of one NVFP4 linear layer Y = X W^T
+    (X [M][K], W [N][K]); see nvfp4_linear_fwd / nvfp4_linear_bwd."""
+
+    def __init__(self, M: int, N: int, K: int, device):
+        self.M, self.N, self.K = M, N, K
+        self.xq = empty_qtensor(M, K, device)
+        self.wq = empty_qtensor(N, K, device)
+        self.wtq = empty_qtensor(K, N, device)
+        self.dyq = empty_qtensor(M, N, device)
+        self.dytq = empty_qtensor(N, M, device)
+        self.xtq = empty_qtensor(K, M, device)
+        self.workspace = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
+
+    def c(self) -> nvfp4_linear_ctx:
+        return nvfp4_linear_ctx(self.M, self.N, self.K, self.xq.c(), self.wq.c(), self.wtq.c(), self.dyq.c(),
+                                self.dytq.c(), self.xtq.c(), self.workspace.data_ptr(), self.workspace.numel())
+
+
+def nvfp4_linear_fwd(X: torch.Tensor, W: torch.Tensor, ctx: LinearContext, Y: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    if Y is None:
+        Y = torch.empty(ctx.M, ctx.N, dtype=torch.bfloat16, device=X.device)
+    for t, shape in ((X, (ctx.M, ctx.K)), (W, (ctx.N, ctx.K)), (Y, (ctx.M, ctx.N))):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"expected contiguous bf16 {shape}, got {t.dtype} {tuple(t.shape)}")
+    c = ctx.c()
+    _check(lib().nvfp4_linear_fwd(X.data_ptr(), W.data_ptr(), Y.data_ptr(), ctypes.byref(c), _stream(stream)),
+           "nvfp4_linear_fwd")
+    return Y
+
+
+def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor, ctx: LinearContext, sr_seed: int, rht_seed: int,
+                     dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None):
+    if dX is None:
+        dX = torch.empty(ctx.M, ctx.K, dtype=torch.bfloat16, device=dY.device)
+    if dW is None:
+        dW = torch.empty(ctx.N, ctx.K, dtype=torch.float32, device=dY.device)
+    for t, shape, dt in ((dY, (ctx.M, ctx.N), torch.bfloat16), (X, (ctx.M, ctx.K), torch.bfloat16),
+                         (dX, (ctx.M, ctx.K), torch.bfloat16), (dW, (ctx.N, ctx.K), torch.float32)):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"expected contiguous {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+    c = ctx.c()
+    _check(lib().nvfp4_linear_bwd(dY.data_ptr(), X.data_ptr(), dX.data_ptr(), dW.data_ptr(), sr_seed, rht_seed,
+                                  ctypes.byref(c), _stream(stream)), "nvfp4_linear_bwd")
+    return dX, dW
+
+
+def nvfp4_sync_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device status code."""
+    return int(lib().nvfp4_sync_status(_stream(stream)))
+
+
+def scales_as_linear(q: QTensor) -> torch.Tensor:
+    """The block scales of q as a [rows][cols/16] uint8 tensor (undoes the
+    MMA layout's index permutation; a pure gather, no arithmetic)."""
+    nkb = q.cols // 16
+    if q.scale_layout == "linear":
+        return q.scales[: q.rows * nkb].view(q.rows, nkb)
+    n_katoms = 4 * ((q.cols + 255) // 256)
+    dev = q.scales.device
+    r = torch.arange(q.rows, device=dev, dtype=torch.int64)[:, None]
+    kb = torch.arange(nkb, device=dev, dtype=torch.int64)[None, :]
+    off = ((r // 128) * n_katoms + kb // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+    return q.scales[off]
+
+
+def codes_view(q: QTensor) -> torch.Tensor:
+    """The packed codes of q without row padding: [rows][cols/2] uint8."""
+    return q.codes[:, : q.cols // 2]

@@ -1,0 +1,381 @@
+// C ABI of the NVFP4 engine: argument checks on the host, then kernel
+// launches on the caller's stream.  See include/nvfp4.h for the contract.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "nvfp4_device.cuh"
+#include "nvfp4_launch.h"
+
+namespace nvfp4 {
+
+// Per-device status word (NVFP4_ERR_NONFINITE / NVFP4_ERR_TIMEOUT bits).
+static __device__ uint32_t g_status_word;
+
+namespace {
+
+thread_local char g_err[512];
+
+nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+nvfp4_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        d.ready = true;
+    }
+    *out = &d;
+    return NVFP4_OK;
+}
+
+nvfp4_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+    return NVFP4_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t n_katoms(int64_t cols) { return 4 * ceil_div(cols, 256); }
+
+size_t scales_bytes(int64_t rows, int64_t cols, int32_t layout) {
+    if (rows < 0 || cols < 0 || cols % 16) return 0;
+    if (layout == NVFP4_SCALES_LINEAR) return (size_t)(rows * (cols / 16));
+    if (layout == NVFP4_SCALES_MMA) return (size_t)(ceil_div(rows, 128) * n_katoms(cols) * 512);
+    return 0;
+}
+
+ScaleOut scale_out(const nvfp4_tensor& t) {
+    ScaleOut s;
+    s.p = t.scales;
+    s.n_katoms = n_katoms(t.cols);
+    s.nkb = t.cols / 16;
+    s.mma = t.scale_layout == NVFP4_SCALES_MMA;
+    return s;
+}
+
+// A quantize output: `rows` x `cols` logical, blocks along cols.
+nvfp4_status check_out(const nvfp4_tensor* t, int64_t rows, int64_t cols, const char* name) {
+    if (!t->codes || !t->scales || !t->amax) return fail(NVFP4_ERR_INVALID_ARG, "%s: null buffer", name);
+    if (t->rows != rows || t->cols != cols)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: shape [%lld][%lld], expected [%lld][%lld]", name, (long long)t->rows,
+                    (long long)t->cols, (long long)rows, (long long)cols);
+    if (cols % 16) return fail(NVFP4_ERR_INVALID_ARG, "%s: cols %lld not a multiple of 16", name, (long long)cols);
+    if (t->ld_codes < cols / 2 || t->ld_codes % 16)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: ld_codes %lld must be >= cols/2 and a multiple of 16", name,
+                    (long long)t->ld_codes);
+    if (t->scale_layout != NVFP4_SCALES_LINEAR && t->scale_layout != NVFP4_SCALES_MMA)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, t->scale_layout);
+    if (t->reserved != 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: reserved field must be 0", name);
+    if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->amax) & 3u))
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: codes/scales must be 16-byte aligned, amax 4-byte aligned", name);
+    return NVFP4_OK;
+}
+
+// Zero the scale buffer when the MMA layout has padding the kernels do not
+// visit (rows to a multiple of 128, K blocks to a multiple of 16).
+nvfp4_status zero_scale_padding(const nvfp4_tensor* t, cudaStream_t s) {
+    if (t->scale_layout != NVFP4_SCALES_MMA) return NVFP4_OK;
+    if (t->rows % 128 == 0 && t->cols % 256 == 0) return NVFP4_OK;
+    cudaError_t e = cudaMemsetAsync(t->scales, 0, scales_bytes(t->rows, t->cols, NVFP4_SCALES_MMA), s);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return NVFP4_OK;
+}
+
+nvfp4_status check_input(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx) {
+    if (!x) return fail(NVFP4_ERR_INVALID_ARG, "x is null");
+    if (dtype != NVFP4_IN_BF16 && dtype != NVFP4_IN_FP32) return fail(NVFP4_ERR_INVALID_ARG, "bad dtype %d", dtype);
+    if (rows <= 0 || cols <= 0) return fail(NVFP4_ERR_INVALID_ARG, "empty input [%lld][%lld]", (long long)rows,
+                                            (long long)cols);
+    if (cols % 16) return fail(NVFP4_ERR_INVALID_ARG, "cols %lld not a multiple of 16", (long long)cols);
+    const int esz = dtype == NVFP4_IN_FP32 ? 4 : 2;
+    if (ldx < cols || (ldx * esz) % 16)
+        return fail(NVFP4_ERR_INVALID_ARG, "ldx %lld must be >= cols and a multiple of 16 bytes", (long long)ldx);
+    if (!aligned16(x)) return fail(NVFP4_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+        return fail(NVFP4_ERR_INVALID_ARG, "input too large");
+    return NVFP4_OK;
+}
+
+nvfp4_status check_workspace(void* ws, size_t bytes) {
+    if (!ws || bytes < (size_t)kMaxPartials * sizeof(uint32_t))
+        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", (size_t)kMaxPartials * 4, bytes);
+    if (!aligned16(ws)) return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    return NVFP4_OK;
+}
+
+int amax_grid(int64_t rows, int64_t cols, int num_sms) {
+    // ~4 vectors of 16 bytes per thread per pass at most; at least one CTA
+    const int64_t vec = rows * cols / 8;
+    int64_t g = ceil_div(vec, (int64_t)kAmaxThreads * 4);
+    g = std::min<int64_t>(g, (int64_t)num_sms * 4);
+    g = std::min<int64_t>(g, kMaxPartials);
+    return (int)std::max<int64_t>(g, 1);
+}
+
+int cap_grid(int64_t units, int per_sm, int num_sms) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)num_sms * per_sm));
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout) {
+    return scales_bytes(rows, cols, scale_layout);
+}
+
+size_t nvfp4_workspace_size(void) { return (size_t)kMaxPartials * sizeof(uint32_t); }
+
+const char* nvfp4_last_error(void) { return g_err; }
+
+const char* nvfp4_status_string(nvfp4_status st) {
+    switch (st) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+        case NVFP4_ERR_UNSUPPORTED: return "unsupported";
+        case NVFP4_ERR_WORKSPACE: return "workspace too small";
+        case NVFP4_ERR_NONFINITE: return "non-finite input";
+        case NVFP4_ERR_TIMEOUT: return "device wait timed out";
+        case NVFP4_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                            nvfp4_block block, nvfp4_round round, uint64_t seed, const nvfp4_tensor* out_rowwise,
+                            const nvfp4_tensor* out_colwise, void* workspace, size_t workspace_bytes,
+                            nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    nvfp4_status st = check_input(x, dtype, rows, cols, ldx);
+    if (st) return st;
+    if (block != NVFP4_BLOCK_1x16 && block != NVFP4_BLOCK_16x16)
+        return fail(NVFP4_ERR_INVALID_ARG, "bad block %d", block);
+    if (round != NVFP4_RTN && round != NVFP4_SR) return fail(NVFP4_ERR_INVALID_ARG, "bad round %d", round);
+    if (!out_rowwise && !out_colwise) return fail(NVFP4_ERR_INVALID_ARG, "no output requested");
+    if (out_rowwise && (st = check_out(out_rowwise, rows, cols, "out_rowwise"))) return st;
+    if (out_colwise) {
+        if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "colwise output needs rows %% 16 == 0");
+        if ((st = check_out(out_colwise, cols, rows, "out_colwise"))) return st;
+    }
+    if (block == NVFP4_BLOCK_16x16) {
+        if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "16x16 blocks need rows %% 16 == 0");
+        if (round != NVFP4_RTN) return fail(NVFP4_ERR_UNSUPPORTED, "16x16 blocks support RTN only");
+    }
+    if ((st = check_workspace(workspace, workspace_bytes))) return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev))) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool fp32 = dtype == NVFP4_IN_FP32;
+    const bool sr = round == NVFP4_SR;
+    uint32_t* partials = static_cast<uint32_t*>(workspace);
+    if (out_rowwise && (st = zero_scale_padding(out_rowwise, s))) return st;
+    if (out_colwise && (st = zero_scale_padding(out_colwise, s))) return st;
+
+    const int ag = amax_grid(rows, cols, dev->num_sms);
+    launch_amax(x, fp32, rows, cols, ldx, partials, ag, s);
+    if ((st = check_launch("amax"))) return st;
+
+    if (block == NVFP4_BLOCK_16x16) {
+        const int g = cap_grid(tiles_2d(rows, cols), 8, dev->num_sms);
+        ScaleOut sr_ = out_rowwise ? scale_out(*out_rowwise) : ScaleOut{};
+        ScaleOut sc_ = out_colwise ? scale_out(*out_colwise) : ScaleOut{};
+        launch_quantize_2d(x, fp32, rows, cols, ldx, partials, ag, out_rowwise ? out_rowwise->codes : nullptr,
+                           out_rowwise ? out_rowwise->ld_codes : 0, sr_, out_rowwise ? out_rowwise->amax : nullptr,
+                           out_colwise ? out_colwise->codes : nullptr, out_colwise ? out_colwise->ld_codes : 0, sc_,
+                           out_colwise ? out_colwise->amax : nullptr, dev->status, g, s);
+        return check_launch("quantize_2d");
+    }
+    if (out_rowwise) {
+        const int64_t groups = rows * ceil_div(cols, 64);
+        const int g = cap_grid(ceil_div(groups, kQuantThreads), 8, dev->num_sms);
+        launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
+                                scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, seed, g, s);
+        if ((st = check_launch("quantize_rowwise"))) return st;
+    }
+    if (out_colwise) {
+        const int g = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
+        launch_quantize_colwise(x, fp32, rows, cols, ldx, partials, ag, out_colwise->codes, out_colwise->ld_codes,
+                                scale_out(*out_colwise), out_colwise->amax, dev->status, sr, seed, false, 0, g, s);
+        if ((st = check_launch("quantize_colwise"))) return st;
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                nvfp4_round round, uint64_t seed, uint64_t rht_seed, const nvfp4_tensor* out_colwise,
+                                void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    nvfp4_status st = check_input(x, dtype, rows, cols, ldx);
+    if (st) return st;
+    if (round != NVFP4_RTN && round != NVFP4_SR) return fail(NVFP4_ERR_INVALID_ARG, "bad round %d", round);
+    if (!out_colwise) return fail(NVFP4_ERR_INVALID_ARG, "out_colwise is null");
+    if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "RHT needs rows %% 16 == 0");
+    if ((st = check_out(out_colwise, cols, rows, "out_colwise"))) return st;
+    if ((st = check_workspace(workspace, workspace_bytes))) return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev))) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool fp32 = dtype == NVFP4_IN_FP32;
+    uint32_t* partials = static_cast<uint32_t*>(workspace);
+    if ((st = zero_scale_padding(out_colwise, s))) return st;
+    const int64_t units = (rows / 16) * (cols / (fp32 ? 4 : 8));
+    const int ag = (int)std::max<int64_t>(
+        1, std::min<int64_t>({ceil_div(units, kAmaxThreads), (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
+    launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
+    if ((st = check_launch("rht_amax"))) return st;
+    const int g = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
+    launch_quantize_colwise(x, fp32, rows, cols, ldx, partials, ag, out_colwise->codes, out_colwise->ld_codes,
+                            scale_out(*out_colwise), out_colwise->amax, dev->status, round == NVFP4_SR, seed, true,
+                            rht_seed, g, s);
+    return check_launch("rht_quantize_colwise");
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,
+                        int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    g_err[0] = 0;
+    if (!A || !B || !C) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    nvfp4_status st;
+    if ((st = check_out(A, A->rows, A->cols, "A")) || (st = check_out(B, B->rows, B->cols, "B"))) return st;
+    if (A->rows <= 0 || B->rows <= 0 || A->cols <= 0) return fail(NVFP4_ERR_INVALID_ARG, "empty GEMM");
+    if (A->cols != B->cols)
+        return fail(NVFP4_ERR_INVALID_ARG, "K mismatch: %lld vs %lld", (long long)A->cols, (long long)B->cols);
+    if (A->cols % 64) return fail(NVFP4_ERR_INVALID_ARG, "K %lld not a multiple of 64", (long long)A->cols);
+    if (A->scale_layout != NVFP4_SCALES_MMA || B->scale_layout != NVFP4_SCALES_MMA)
+        return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands need NVFP4_SCALES_MMA");
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+        return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
+    const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldc < B->rows || (ldc * esz) % 16 || !aligned16(C))
+        return fail(NVFP4_ERR_INVALID_ARG, "C: ldc must be >= N and 16-byte rows, C 16-byte aligned");
+    DeviceInfo* dev;
+    if ((st = device_info(&dev))) return st;
+    GemmArgs g;
+    g.a_codes = A->codes;
+    g.a_scales = A->scales;
+    g.a_amax = A->amax;
+    g.lda = A->ld_codes;
+    g.b_codes = B->codes;
+    g.b_scales = B->scales;
+    g.b_amax = B->amax;
+    g.ldb = B->ld_codes;
+    g.c = C;
+    g.ldc = ldc;
+    g.M = A->rows;
+    g.N = B->rows;
+    g.K = A->cols;
+    g.out_fp32 = out_dtype == NVFP4_OUT_FP32;
+    g.status = dev->status;
+    g.num_sms = dev->num_sms;
+    const char* msg = nullptr;
+    int e = launch_gemm(g, reinterpret_cast<cudaStream_t>(stream), &msg);
+    if (e == -1) return fail(NVFP4_ERR_UNSUPPORTED, "gemm: %s", msg ? msg : "unsupported");
+    if (e) return fail(NVFP4_ERR_CUDA, "gemm: %s", msg ? msg : cudaGetErrorString((cudaError_t)e));
+    return check_launch("gemm");
+}
+
+static nvfp4_status check_linear_tensor(const nvfp4_tensor* t, int64_t rows, int64_t cols, const char* name) {
+    nvfp4_status st = check_out(t, rows, cols, name);
+    if (st) return st;
+    if (t->scale_layout != NVFP4_SCALES_MMA) return fail(NVFP4_ERR_INVALID_ARG, "%s: needs NVFP4_SCALES_MMA", name);
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    if (!ctx || !X || !W || !Y) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    const int64_t M = ctx->M, N = ctx->N, K = ctx->K;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 64 || N % 64 || K % 64)
+        return fail(NVFP4_ERR_INVALID_ARG, "M, N, K must be positive multiples of 64");
+    nvfp4_status st;
+    if ((st = check_linear_tensor(&ctx->xq, M, K, "xq")) || (st = check_linear_tensor(&ctx->wq, N, K, "wq")) ||
+        (st = check_linear_tensor(&ctx->wtq, K, N, "wtq")))
+        return st;
+    if ((st = nvfp4_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_BLOCK_1x16, NVFP4_RTN, 0, &ctx->xq, nullptr,
+                             ctx->workspace, ctx->workspace_bytes, stream)))
+        return st;
+    if ((st = nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq,
+                             ctx->workspace, ctx->workspace_bytes, stream)))
+        return st;
+    return nvfp4_gemm(&ctx->xq, &ctx->wq, Y, NVFP4_OUT_BF16, N, nullptr, 0, stream);
+}
+
+nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,
+                              uint64_t rht_seed, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    if (!ctx || !dY || !X || !dX || !dW) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    const int64_t M = ctx->M, N = ctx->N, K = ctx->K;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 64 || N % 64 || K % 64)
+        return fail(NVFP4_ERR_INVALID_ARG, "M, N, K must be positive multiples of 64");
+    nvfp4_status st;
+    if ((st = check_linear_tensor(&ctx->wtq, K, N, "wtq")) || (st = check_linear_tensor(&ctx->dyq, M, N, "dyq")) ||
+        (st = check_linear_tensor(&ctx->dytq, N, M, "dytq")) || (st = check_linear_tensor(&ctx->xtq, K, M, "xtq")))
+        return st;
+    // Dgrad: dX = dY W with SR gradients and the 16x16 weight codes of W^T
+    if ((st = nvfp4_quantize(dY, NVFP4_IN_BF16, M, N, N, NVFP4_BLOCK_1x16, NVFP4_SR, sr_seed, &ctx->dyq, nullptr,
+                             ctx->workspace, ctx->workspace_bytes, stream)))
+        return st;
+    if ((st = nvfp4_gemm(&ctx->dyq, &ctx->wtq, dX, NVFP4_OUT_BF16, K, nullptr, 0, stream))) return st;
+    // Wgrad: dW = dY^T X with both operands transformed along the tokens
+    if ((st = nvfp4_rht_quantize(dY, NVFP4_IN_BF16, M, N, N, NVFP4_SR, sr_seed, rht_seed, &ctx->dytq,
+                                 ctx->workspace, ctx->workspace_bytes, stream)))
+        return st;
+    if ((st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
+                                 ctx->workspace_bytes, stream)))
+        return st;
+    return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, NVFP4_OUT_FP32, K, nullptr, 0, stream);
+}
+
+nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    uint32_t word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemcpyFromSymbol: %s", cudaGetErrorString(e));
+    if (word) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemcpyToSymbol: %s", cudaGetErrorString(e));
+    }
+    if (word & kStatusTimeout) return fail(NVFP4_ERR_TIMEOUT, "a device wait ran out of iterations");
+    if (word & kStatusNonfinite) return fail(NVFP4_ERR_NONFINITE, "input held a NaN or an infinity");
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+// Device-side building blocks of the NVFP4 quantizer (sm_103a).
+//
+// Format ("Pretraining Large Language Models with NVFP4", summary page,
+// format paragraph): E2M1 elements, one E4M3 scale per 16 elements, one FP32
+// scale per tensor.  Every FP32 step below is a single correctly rounded
+// operation (explicit __f*_rn intrinsics, so no contraction into FMA).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+constexpr float kTensorRange = 2688.0f;  // E2M1 max (6) * E4M3 max (448)
+constexpr float kFltMax = 3.402823466e+38f;
+
+// Bits of the per-device status word.
+constexpr uint32_t kStatusNonfinite = 1u;
+constexpr uint32_t kStatusTimeout = 2u;
+
+// ---------------------------------------------------------------------------
+// Tensor scales from the tensor amax A (given as the bit pattern of |A|).
+struct TensorScales {
+    float amax, s_dec, s_enc;
+    bool finite;
+};
+
+__device__ __forceinline__ TensorScales tensor_scales_from_bits(uint32_t amax_bits) {
+    TensorScales t;
+    t.finite = amax_bits < 0x7f800000u;
+    t.amax = __uint_as_float(amax_bits);
+    if (!t.finite || amax_bits == 0u) {
+        t.s_dec = 1.0f;
+        t.s_enc = 1.0f;
+        if (!t.finite) t.amax = __uint_as_float(amax_bits);
+        return t;
+    }
+    t.s_dec = __fdiv_rn(t.amax, kTensorRange);
+    float e = __fdiv_rn(kTensorRange, t.amax);
+    t.s_enc = isinf(e) ? kFltMax : e;
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 block scale: sb = E4M3_rne_satfinite(fl(fl(bamax / 6) * S_enc)).
+__device__ __forceinline__ uint32_t e4m3_from_float(float v) {
+    uint16_t out;
+    // v goes to the low byte (second source operand)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(v));
+    return out & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+    // unsigned use only: normal (1 + m/8) 2^(e-7) re-biased into FP32, or
+    // subnormal m * 2^-9
+    return (b & 0x78u) ? __uint_as_float(((b & 0x7Fu) << 20) + (120u << 23))
+                       : __fmul_rn((float)(b & 7u), 0.001953125f);
+}
+
+struct BlockScale {
+    uint32_t sb;  // E4M3 code (0 = all codes zero)
+    float r;      // per-element multiplier S_enc / sb
+};
+
+__device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc) {
+    BlockScale b;
+    float t = __fdiv_rn(bamax, 6.0f);
+    b.sb = e4m3_from_float(__fmul_rn(t, s_enc));
+    float r = __fdiv_rn(s_enc, e4m3_to_float(b.sb));
+    b.r = isinf(r) ? kFltMax : r;
+    if (b.sb == 0u) b.r = 0.0f;
+    return b;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 round to nearest (ties to even), saturating, two at a time.  The
+// hardware conversion places its first source operand in the high nibble,
+// so element 2j (low nibble) is the second operand.  The sign bit of each
+// input is OR-ed in so that negative values rounding to 0 keep code 0x8.
+__device__ __forceinline__ uint32_t e2m1x8_rtn(const float v[8]) {
+    uint32_t out;
+    asm("{\n\t"
+        ".reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+        "}"
+        : "=r"(out)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    uint32_t signs = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) signs |= (__float_as_uint(v[j]) >> 31) << (4 * j + 3);
+    return out | signs;
+}
+
+// E2M1 stochastic rounding of one value with its 32-bit random word: the
+// magnitude (saturated at 6) goes up to the next grid point iff
+// (rbits >> 8) * 2^-24 < frac, frac = (|v| - lo) / (hi - lo) (exact).
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t rbits) {
+    uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
+    float a = fminf(fabsf(v), 6.0f);
+    // scale the binade so the grid spacing becomes 1: [0,2) x2, [2,4) x1, [4,6] x0.5
+    float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+    float t = __fmul_rn(a, s);
+    float k = floorf(t);
+    float frac = __fsub_rn(t, k);
+    uint32_t code_lo = a < 2.0f ? (uint32_t)k : (a < 4.0f ? (uint32_t)k + 2u : 6u);
+    uint32_t up = ((float)(rbits >> 8) < __fmul_rn(frac, 16777216.0f)) ? 1u : 0u;
+    uint32_t code = a >= 6.0f ? 7u : code_lo + up;
+    return sign | code;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Random words of elements i0..i0+3 (i0 % 4 == 0) of a logical tensor for
+// stochastic rounding: counter (i0/4 low, i0/4 high, 0, 0), key = seed.
+__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t i0) {
+    uint64_t q = i0 >> 2;
+    return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+
+// Encode 16 consecutive elements of one block (already multiplied by r) into
+// 8 bytes.  SR: i0 is the logical index of element 0 (multiple of 16).
+template <bool kSR>
+__device__ __forceinline__ uint2 encode16(const float v[16], uint64_t seed, uint64_t i0) {
+    uint2 out;
+    if constexpr (!kSR) {
+        out.x = e2m1x8_rtn(v);
+        out.y = e2m1x8_rtn(v + 8);
+    } else {
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 r = sr_words(seed, i0 + 4 * q);
+            uint32_t c0 = e2m1_sr(v[4 * q + 0], r.x), c1 = e2m1_sr(v[4 * q + 1], r.y);
+            uint32_t c2 = e2m1_sr(v[4 * q + 2], r.z), c3 = e2m1_sr(v[4 * q + 3], r.w);
+            uint32_t nib = c0 | (c1 << 4) | (c2 << 8) | (c3 << 12);
+            w[q >> 1] |= nib << (16 * (q & 1));
+        }
+        out.x = w[0];
+        out.y = w[1];
+    }
+    return out;
+}
+
+// ---------------------------------------------------------------------------
+// 16-point random Hadamard transform of one chunk, in place:
+// y = (1/4) H16 (d . x), stages over index bits 0, 1, 2, 3, each sum rounded.
+// `dmask` bit j set means d_j = -1.
+__device__ __forceinline__ void rht16(float x[16], uint32_t dmask) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if ((dmask >> j) & 1u) x[j] = -x[j];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int h = 1 << s;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j & h) continue;
+            float a = x[j], b = x[j + h];
+            x[j] = __fadd_rn(a, b);
+            x[j + h] = __fsub_rn(a, b);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], 0.25f);
+}
+
+__device__ __forceinline__ uint32_t rht_sign_mask(uint64_t rht_seed) {
+    uint4 w = philox4x32_10(make_uint4(0u, 0u, 1u, 0u), (uint32_t)rht_seed, (uint32_t)(rht_seed >> 32));
+    return w.x & 0xFFFFu;
+}
+
+// ---------------------------------------------------------------------------
+// Scale-buffer addressing (see nvfp4.h, NVFP4_SCALES_MMA).
+__device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t n_katoms) {
+    return ((r >> 7) * n_katoms + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+struct ScaleOut {
+    uint8_t* p;
+    int64_t n_katoms;  // MMA layout
+    int64_t nkb;       // linear layout: blocks per row (cols / 16)
+    int mma;
+    __device__ __forceinline__ int64_t offset(int64_t r, int64_t kb) const {
+        return mma ? mma_scale_offset(r, kb, n_katoms) : r * nkb + kb;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Element loads.  Input rows are 16-byte aligned.
+template <typename T>
+struct In;
+
+template <>
+struct In<__nv_bfloat16> {
+    static constexpr int kVec = 8;  // elements per 16-byte load
+    __device__ __forceinline__ static void load8(const __nv_bfloat16* p, float f[8]) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(w[j] << 16);
+            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+};
+
+template <>
+struct In<float> {
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void load8(const float* p, float f[8]) {
+        float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+};
+
+__device__ __forceinline__ uint32_t abs_bits(float f) { return __float_as_uint(f) & 0x7FFFFFFFu; }
+
+}  // namespace nvfp4

@@ -1,0 +1,55 @@
+// Host-side launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+constexpr int kAmaxThreads = 512;
+constexpr int kQuantThreads = 256;
+constexpr int kColThreads = 128;
+constexpr int k2dThreads = 256;
+constexpr int kMaxPartials = 2048;  // workspace holds one uint32 partial max per amax CTA
+
+struct ScaleOut;
+
+void launch_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint32_t* partials, int grid,
+                 cudaStream_t s);
+void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
+                     uint32_t* partials, int grid, cudaStream_t s);
+void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
+                             const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
+                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, int grid, cudaStream_t s);
+void launch_quantize_colwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
+                             const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
+                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, bool rht, uint64_t rht_seed,
+                             int grid, cudaStream_t s);
+void launch_quantize_2d(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* partials,
+                        int npartials, uint8_t* codes_r, int64_t ld_r, ScaleOut so_r, float* amax_r, uint8_t* codes_c,
+                        int64_t ld_c, ScaleOut so_c, float* amax_c, uint32_t* status, int grid, cudaStream_t s);
+int64_t colwise_tiles(int64_t rows, int64_t cols);
+int64_t tiles_2d(int64_t rows, int64_t cols);
+
+// GEMM (gemm.cu).  A: [M][K] codes/scales (MMA layout), B: [N][K].
+struct GemmArgs {
+    const uint8_t* a_codes;
+    const uint8_t* a_scales;
+    const float* a_amax;
+    int64_t lda;  // bytes
+    const uint8_t* b_codes;
+    const uint8_t* b_scales;
+    const float* b_amax;
+    int64_t ldb;  // bytes
+    void* c;
+    int64_t ldc;  // elements
+    int64_t M, N, K;
+    int out_fp32;
+    uint32_t* status;
+    int num_sms;
+};
+
+// Returns a cudaError_t-like code (0 ok) and fills `msg` on failure.
+int launch_gemm(const GemmArgs& args, cudaStream_t s, const char** msg);
+
+}  // namespace nvfp4

@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/nvfp4.h declares; host-side argument checks answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(nvfp4_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantize_block_scaled_amax_gb300 import build
+    build.build()
+    import quantize_block_scaled_amax_gb300 as q
+    return q.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
+                     "nvfp4_sync_status", "nvfp4_status_string", "nvfp4_workspace_size", "nvfp4_scales_bytes",
+                     "nvfp4_last_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_struct_layout_matches_header(L):
+    import quantize_block_scaled_amax_gb300 as q
+    # nvfp4_tensor: 3 pointers, 3 int64, 2 int32 = 56 bytes on LP64
+    assert ctypes.sizeof(q.nvfp4_tensor) == 56
+    assert ctypes.sizeof(q.nvfp4_linear_ctx) == 3 * 8 + 6 * 56 + 8 + 8
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.nvfp4_status_string(code)
+    assert L.nvfp4_status_string(4) == b"non-finite input"
+
+
+def test_scales_bytes(L):
+    import quantize_block_scaled_amax_gb300 as q
+    # linear: one byte per 1x16 block
+    assert q.nvfp4_scales_bytes(8192, 5120, "linear") == 8192 * 320
+    # MMA layout: 128-row groups x 4*ceil(K/256) atoms of 512 bytes
+    assert q.nvfp4_scales_bytes(8192, 5120, "mma") == 64 * 80 * 512
+    assert q.nvfp4_scales_bytes(200, 320, "mma") == 2 * 8 * 512
+    assert q.nvfp4_scales_bytes(16, 17, "mma") == 0          # cols not a multiple of 16
+    assert q.nvfp4_workspace_size() >= 4096
+
+
+def test_host_argument_checks_need_no_gpu(L):
+    # every call below must fail its host-side checks before any launch: the
+    # pointers are placeholders, never dereferenced
+    import quantize_block_scaled_amax_gb300 as q
+    t = q.nvfp4_tensor(16, 16, 16, 16, 32, 16, 1, 0)
+    # null input
+    assert L.nvfp4_quantize(None, 0, 16, 32, 32, 0, 0, 0, ctypes.byref(t), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # cols not a multiple of 16
+    assert L.nvfp4_quantize(16, 0, 16, 24, 24, 0, 0, 0, ctypes.byref(t), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # empty input
+    assert L.nvfp4_quantize(16, 0, 0, 32, 32, 0, 0, 0, ctypes.byref(t), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # no output
+    assert L.nvfp4_quantize(16, 0, 16, 32, 32, 0, 0, 0, None, None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # misaligned input pointer
+    assert L.nvfp4_quantize(24, 0, 16, 32, 32, 0, 0, 0, ctypes.byref(t), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # output shape mismatch
+    bad = q.nvfp4_tensor(16, 16, 16, 16, 64, 32, 1, 0)
+    assert L.nvfp4_quantize(16, 0, 16, 32, 32, 0, 0, 0, ctypes.byref(bad), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    # 16x16 with SR is not offered
+    assert L.nvfp4_quantize(16, 0, 16, 32, 32, 1, 1, 0, ctypes.byref(t), None, 16, 8192, None) == q.ERR_UNSUPPORTED
+    # workspace too small
+    assert L.nvfp4_quantize(16, 0, 16, 32, 32, 0, 0, 0, ctypes.byref(t), None, 16, 64, None) == q.ERR_WORKSPACE
+    assert b"workspace" in L.nvfp4_last_error()
+    # RHT needs rows % 16 == 0
+    tc2 = q.nvfp4_tensor(16, 16, 16, 32, 24, 16, 1, 0)
+    assert L.nvfp4_rht_quantize(16, 0, 24, 32, 32, 0, 0, 0, ctypes.byref(tc2), 16, 8192, None) == q.ERR_INVALID_ARG
+
+
+def test_gemm_argument_checks_need_no_gpu(L):
+    import quantize_block_scaled_amax_gb300 as q
+    a = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 1, 0)
+    b = q.nvfp4_tensor(16, 16, 16, 64, 64, 32, 1, 0)      # K mismatch
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
+    b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 0, 0)     # linear scales
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
+    a = q.nvfp4_tensor(16, 16, 16, 128, 96, 48, 1, 0)     # K % 64 != 0
+    b = q.nvfp4_tensor(16, 16, 16, 64, 96, 48, 1, 0)
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
