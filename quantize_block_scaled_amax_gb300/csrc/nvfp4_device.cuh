@@ -76,20 +76,26 @@ __device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc) {
 // ---------------------------------------------------------------------------
 // E2M1 round to nearest (ties to even), saturating, two at a time.  The
 // hardware conversion places its first source operand in the high nibble,
-// so element 2j (low nibble) is the second operand.  The sign bit of each
-// input is OR-ed in so that negative values rounding to 0 keep code 0x8.
+// so element 2j (low nibble) is the second operand.  Each 8-bit result is
+// widened on its own (cvt.u32.u8) before packing: packing four 8-bit
+// registers with one vector mov produced wrong bytes inside the 16x16
+// kernel with this toolchain.  The sign bit of each input is OR-ed in so
+// that negative values rounding to 0 keep code 0x8.
+__device__ __forceinline__ uint32_t e2m1x2_rtn(float lo, float hi) {
+    uint32_t h;
+    asm volatile(
+        "{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(h)
+        : "f"(hi), "f"(lo));
+    return h & 0xFFu;
+}
+
 __device__ __forceinline__ uint32_t e2m1x8_rtn(const float v[8]) {
-    uint32_t out;
-    asm("{\n\t"
-        ".reg .b8 b0, b1, b2, b3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-        "mov.b32 %0, {b0, b1, b2, b3};\n\t"
-        "}"
-        : "=r"(out)
-        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    uint32_t out = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out |= e2m1x2_rtn(v[2 * j], v[2 * j + 1]) << (8 * j);
     uint32_t signs = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) signs |= (__float_as_uint(v[j]) >> 31) << (4 * j + 3);

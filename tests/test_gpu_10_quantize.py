@@ -265,6 +265,7 @@ def test_full_size_gradient_sr_and_rht(nv):
     for rows in _row_samples(5120):
         assert_quant_equal(xt, oracle.quantize(xn, layout="col", rht_seed=workloads.RHT_SEED, rows=rows, logical=lx),
                            rows=rows, what=f"X^T RHT RTN {rows}")
-    # many block scales of the heavy-tailed gradient are E4M3 subnormals
+    # heavy tails: the block holding the tensor max gets the top scale (448)
+    # while the typical block scale sits far below it
     s = scales_np(dyr)
-    assert (s[s > 0] < 8).mean() > 0.001
+    assert s.max() == 0x7E and np.median(s) < 0x60
