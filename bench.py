@@ -1,0 +1,517 @@
+"""Benchmark of the NVFP4 linear-layer hot path on GB300.
+
+One step = one NVFP4 linear layer forward + backward at the 12B model's FFN
+up-projection shape (M = 8192 tokens, N = 20480, K = 5120), through the C ABI:
+  Fprop : amax + 1x16 RTN quantize of X; amax + 16x16 RTN quantize of W (both
+          layouts); GEMM Y = Xq Wq^T (bf16 out)
+  Dgrad : amax + 1x16 SR quantize of dY; GEMM dX = dYq Wq (bf16 out)
+  Wgrad : RHT amax + RHT 1x16 SR colwise quantize of dY; RHT amax + RHT RTN
+          colwise quantize of X; GEMM dW = (H dY)^T (H X) (fp32 out)
+value = GEMM FLOPs of the step (3 x 2MNK) / step time (quantization included).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+With N > 1 (launched by torchrun) every rank runs an independent replica of
+the step (weak scaling); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K = 8192, 20480, 5120
+METRIC = "NVFP4 GEMM TFLOPS (8192x20480x5120) and quantize+RHT GB/s vs roofline"
+UNIT = "TFLOP/s"
+WORKLOAD = ("NVFP4 linear layer fwd+bwd (Fprop+Dgrad+Wgrad GEMMs with all quantizations), "
+            "X 8192x5120, W 20480x5120, dY 8192x20480 bf16; 12B hybrid model FFN up-projection at seq 8192")
+FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 / BF16 tensor rate on GB300
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0, source="fallback")
+
+
+# ---- profile summaries: DRAM traffic of the dominant kernel ------------------------
+
+def _profile_traffic(kernel_file: str, summary: str):
+    """Bytes per launch from a committed ncu summary, or None if the summary is
+    missing or was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(" "):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = open(os.path.join(ROOT, "quantize_block_scaled_amax_gb300", "csrc", kernel_file), "rb").read()
+    if fields.get("source_sha256", "") != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---- clocks ---------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(self._path(), "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _path(self):
+        d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+        return os.path.join(d, f"bench_clocks_{os.getpid()}.csv")
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self._path()):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]), active=parts[4],
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7], sw_power=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---- the GPU step -------------------------------------------------------------------
+
+def gpu_bench(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local_rank = _env_rank()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from quantize_block_scaled_amax_gb300 import build as _b
+    _b.build()
+    import quantize_block_scaled_amax_gb300 as nv
+    import workloads
+
+    x = workloads.activations(M, K, device=dev)
+    w = workloads.weights(N, K, device=dev)
+    dy = workloads.gradients(M, N, device=dev)
+    ctx = nv.LinearContext(M, N, K, dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+
+    # the step, op by op through the C ABI (the same calls nvfp4_linear_fwd/bwd make)
+    ops = [
+        ("quant_x_1x16_rtn", lambda: nv.nvfp4_quantize(x, out_rowwise=ctx.xq)),
+        ("quant_w_16x16_both", lambda: nv.nvfp4_quantize(w, block="16x16", colwise=True, out_rowwise=ctx.wq,
+                                                         out_colwise=ctx.wtq)),
+        ("gemm_fprop", lambda: nv.nvfp4_gemm(ctx.xq, ctx.wq, out=y)),
+        ("quant_dy_1x16_sr", lambda: nv.nvfp4_quantize(dy, round="sr", seed=sr, out_rowwise=ctx.dyq)),
+        ("gemm_dgrad", lambda: nv.nvfp4_gemm(ctx.dyq, ctx.wtq, out=dx)),
+        ("rht_quant_dy_sr", lambda: nv.nvfp4_rht_quantize(dy, round="sr", seed=sr, rht_seed=rh, out_colwise=ctx.dytq)),
+        ("rht_quant_x_rtn", lambda: nv.nvfp4_rht_quantize(x, round="rtn", rht_seed=rh, out_colwise=ctx.xtq)),
+        ("gemm_wgrad", lambda: nv.nvfp4_gemm(ctx.dytq, ctx.xtq, out=dw)),
+    ]
+    launches_per_op = {"quant_x_1x16_rtn": 2, "quant_w_16x16_both": 2, "gemm_fprop": 1, "quant_dy_1x16_sr": 2,
+                       "gemm_dgrad": 1, "rht_quant_dy_sr": 2, "rht_quant_x_rtn": 2, "gemm_wgrad": 1}
+    # algorithmic bytes: the amax pass reads the input once, the encode pass
+    # reads it again and writes codes (1/2 byte per element) and one E4M3
+    # scale per 16 elements per layout
+    bx, bw, bdy = M * K * 2, N * K * 2, M * N * 2
+    op_bytes = {
+        "quant_x_1x16_rtn": 2 * bx + M * K // 2 + M * K // 16,
+        "quant_w_16x16_both": 2 * bw + 2 * (N * K // 2 + N * K // 16),
+        "quant_dy_1x16_sr": 2 * bdy + M * N // 2 + M * N // 16,
+        "rht_quant_dy_sr": 2 * bdy + M * N // 2 + M * N // 16,
+        "rht_quant_x_rtn": 2 * bx + M * K // 2 + M * K // 16,
+    }
+    gemm_flops = 2.0 * M * N * K
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize()
+    st = nv.nvfp4_sync_status()
+    if st != nv.OK:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)                  # evict L2 between steps (not timed)
+        for (name, fn), (e0, e1) in zip(ops, evs[s]):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+
+    per_op = {name: 0.0 for name, _ in ops}
+    for s in range(args.steps):
+        for (name, _), (e0, e1) in zip(ops, evs[s]):
+            per_op[name] += e0.elapsed_time(e1)
+    total_ms = max_over_ranks(sum(per_op.values()), dev)
+    ms_per_step = total_ms / args.steps
+    value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd/bwd
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        wh = w.cpu().pin_memory()
+        dyh = dy.cpu().pin_memory()
+        yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+        dxh = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
+        dwh = torch.empty(N, K, dtype=torch.float32).pin_memory()
+        xd, wd, dyd = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            wd.copy_(wh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+            nv.nvfp4_linear_fwd(xd, wd, ctx, Y=y)
+            nv.nvfp4_linear_bwd(dyd, xd, ctx, sr_seed=sr, rht_seed=rh, dX=dx, dW=dw)
+            yh.copy_(y, non_blocking=True)
+            dxh.copy_(dx, non_blocking=True)
+            dwh.copy_(dw, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, args.steps // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, dev)
+        e2e = {"value": round(world * 3 * gemm_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "ms_per_step": round(e2e_ms, 4),
+               "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2 + dyh.numel() * 2),
+               "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2 + dwh.numel() * 4),
+               "api": "nvfp4_linear_fwd + nvfp4_linear_bwd, pinned host buffers"}
+    st = nv.nvfp4_sync_status()
+    if st != nv.OK:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return None
+
+    peaks = _peaks()
+    fp4_peak = peaks["bf16_sustained"] * FP4_OVER_BF16
+    kernels = {}
+    for name, ms in per_op.items():
+        avg = ms / args.steps
+        if name.startswith("gemm"):
+            ach = gemm_flops / (avg * 1e-3) / 1e12
+            kernels[name] = {"ms": round(avg, 4), "tflops": round(ach, 1), "frac": round(ach / fp4_peak, 4)}
+        else:
+            ach = op_bytes[name] / (avg * 1e-3) / 1e9
+            kernels[name] = {"ms": round(avg, 4), "gbs": round(ach, 1), "frac": round(ach / peaks["hbm"], 4),
+                             "bytes": op_bytes[name]}
+    gemm_ms = sum(v["ms"] for k, v in kernels.items() if k.startswith("gemm"))
+    quant_ms = sum(v["ms"] for k, v in kernels.items() if not k.startswith("gemm"))
+    quant_bytes = sum(op_bytes.values())
+    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    gemm_avg_ms = gemm_ms / 3
+    gemm_ach = gemm_flops / (gemm_avg_ms * 1e-3) / 1e12
+    roof_gemm = {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                 "frac": round(gemm_ach / fp4_peak, 4),
+                 "traffic": _profile_traffic("gemm.cu", "gemm_nvf4_fprop_8192x20480x5120.txt"),
+                 "kernel": "nvf4_gemm_kernel (avg of Fprop, Dgrad, Wgrad launches)",
+                 "peak_source": f"{peaks['source']} sustained bf16 {peaks['bf16_sustained']} TFLOP/s x "
+                                f"{FP4_OVER_BF16:g} (nominal FP4/BF16 ratio)"}
+    roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                  "frac": round(quant_gbs / peaks["hbm"], 4), "traffic": None,
+                  "kernel": "all quantize + RHT launches of the step (amax pass + encode pass)",
+                  "peak_source": f"{peaks['source']} HBM copy bandwidth"}
+    dominant_is_gemm = gemm_ms >= quant_ms
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate; fp32 quantize)",
+        "data": "synthetic (seeded: X N(0,1)+0.1% x50 outliers, W N(0,0.02), dY Student-t(3)*1e-3)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "l2": "flushed between steps (256 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "quantize_rht_gbs": round(quant_gbs, 1),
+        "gemm_tflops": round(gemm_ach, 1),
+        "roofline": roof_gemm if dominant_is_gemm else roof_quant,
+        "roofline_quantize": roof_quant,
+        "roofline_gemm": roof_gemm,
+        "kernels": kernels,
+        "share": {"gemm": round(gemm_ms / (gemm_ms + quant_ms), 4), "quantize": round(quant_ms / (gemm_ms + quant_ms), 4)},
+        "gpu_launches": args.steps * sum(launches_per_op.values()),
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_subprocess(args.cpu_sample_m, args.cpu_sample_n)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return out
+
+
+# ---- the oracle on the host cores ----------------------------------------------------
+
+def oracle_inputs(m: int, n: int, k: int):
+    """Seeded inputs of a bounded sample of the layer: m tokens, n output
+    features, the full K."""
+    import workloads
+    x = workloads.activations(m, k, seed=workloads.SEED_BASE + 10).float().numpy()
+    w = workloads.weights(n, k, seed=workloads.SEED_BASE + 11).float().numpy()
+    dy = workloads.gradients(m, n, seed=workloads.SEED_BASE + 12).float().numpy()
+    return x, w, dy
+
+
+def oracle_step(x, w, dy):
+    """The step computed by the oracle: every quantization of the recipe and
+    the three GEMMs (FP64 products of the dequantized operands)."""
+    import numpy as np
+    import oracle
+    import workloads
+
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    qx = oracle.quantize(x)
+    qw = oracle.quantize(w, block="16x16")
+    qwt = oracle.quantize(w, layout="col", block="16x16")
+    y = oracle.gemm(qx, qw)
+    qdy = oracle.quantize(dy, rounding="sr", seed=sr)
+    dx = oracle.gemm(qdy, qwt)
+    qdyt = oracle.quantize(dy, layout="col", rounding="sr", seed=sr, rht_seed=rh)
+    qxt = oracle.quantize(x, layout="col", rht_seed=rh)
+    dw = oracle.gemm(qdyt, qxt)
+    return float(np.abs(y).sum() + np.abs(dx).sum() + np.abs(dw).sum())
+
+
+def _oracle_sample_desc(m, n):
+    return (f"oracle step on a {m}-token x {n}-feature slice of the layer at K={K} "
+            f"(quantize X, W 16x16 both layouts, dY SR, RHT dY^T SR, RHT X^T; Fprop, Dgrad, Wgrad FP64 GEMMs); "
+            f"value = 3*2*{m}*{n}*{K} FLOP / oracle time")
+
+
+def cpu_baseline_subprocess(m: int, n: int):
+    """Time the oracle in a fresh single-threaded process (no fork after CUDA)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--cpu-sample-m", str(m),
+                        "--cpu-sample-n", str(n)], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _single_thread():
+    # must run before numpy / torch load their thread pools
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+
+
+def cpu_baseline_only(m: int, n: int):
+    import torch
+    torch.set_num_threads(1)
+    import oracle
+    oracle.build()
+    oracle_step(*oracle_inputs(16, 64, K))          # load and warm the library
+    inputs = oracle_inputs(m, n, K)
+    t0 = time.perf_counter()
+    oracle_step(*inputs)
+    dt = time.perf_counter() - t0
+    flops = 3 * 2.0 * m * n * K
+    print(json.dumps({"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                      "seconds": round(dt, 3), "sample": _oracle_sample_desc(m, n)}))
+
+
+def reference_arm(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return None
+    import torch
+    torch.set_num_threads(1)
+    import oracle
+    oracle.build()
+    m, n = args.ref_sample_m, args.ref_sample_n
+    inputs = oracle_inputs(m, n, K)
+    for _ in range(args.warmup):
+        oracle_step(*inputs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(*inputs)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 3 * 2.0 * m * n * K / dt / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle: FP32 steps emulated in FP64, FP64 GEMM)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
+                                        "sample": _oracle_sample_desc(m, n)},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": _oracle_sample_desc(m, n)},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def profile_case(args):
+    """One launch of one op of the step, for profiler captures: setup (input
+    generation, quantization of the operands) runs first, then the op once."""
+    import torch
+    from quantize_block_scaled_amax_gb300 import build as _b
+    _b.build()
+    import quantize_block_scaled_amax_gb300 as nv
+    import workloads
+    m, n, k = args.m or M, args.n or N, args.k or K
+    dev = torch.device("cuda", 0)
+    op = args.profile
+    if op.startswith("gemm"):
+        x = workloads.activations(m, k, device=dev)
+        w = workloads.weights(n, k, device=dev)
+        qx, _ = nv.nvfp4_quantize(x)
+        qw, _ = nv.nvfp4_quantize(w, block="16x16")
+        del x, w
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_gemm(qx, qw, out=y)
+    elif op == "quant_x_rtn":
+        x = workloads.activations(m, k, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_quantize(x)
+    elif op == "quant_w_2d":
+        w = workloads.weights(n, k, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_quantize(w, block="16x16", colwise=True)
+    elif op == "quant_dy_sr":
+        dy = workloads.gradients(m, n, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_quantize(dy, round="sr", seed=workloads.SR_SEED)
+    elif op == "rht_dy_sr":
+        dy = workloads.gradients(m, n, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_rht_quantize(dy, round="sr", seed=workloads.SR_SEED, rht_seed=workloads.RHT_SEED)
+    else:
+        raise SystemExit(f"unknown profile op {op}")
+    torch.cuda.synchronize()
+    st = nv.nvfp4_sync_status()
+    if st != nv.OK:
+        raise SystemExit(f"device status {st}")
+    print(json.dumps({"profile": op, "m": m, "n": n, "k": k, "status": "ok"}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-only", action="store_true")
+    ap.add_argument("--cpu-sample-m", type=int, default=512)
+    ap.add_argument("--cpu-sample-n", type=int, default=4096)
+    ap.add_argument("--profile", default=None,
+                    help="run one launch of one op: gemm_fprop, quant_x_rtn, quant_w_2d, quant_dy_sr, rht_dy_sr")
+    ap.add_argument("--m", type=int, default=0)
+    ap.add_argument("--n", type=int, default=0)
+    ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--ref-sample-m", type=int, default=64)
+    ap.add_argument("--ref-sample-n", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.cpu_baseline_only or args.impl == "reference":
+        _single_thread()
+    if args.cpu_baseline_only:
+        cpu_baseline_only(args.cpu_sample_m, args.cpu_sample_n)
+        return
+    if args.profile:
+        profile_case(args)
+        return
+    out = reference_arm(args) if args.impl == "reference" else gpu_bench(args)
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()
