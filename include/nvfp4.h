@@ -137,6 +137,33 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
                             void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is an interface
+ * convenience, not part of the method.
+ *   Some callers have no way to get the 8 KB workspace nvfp4_quantize asks
+ *   for: a plugin or extension whose host framework owns every device
+ *   allocation and offers it no allocation hook, or a real-time loop that
+ *   must not call cudaMalloc after set-up (cudaMalloc can synchronize the
+ *   device and can fail once memory is fragmented).  This entry point keeps
+ *   the amax partials in a fixed 8 KB device array inside the library and
+ *   allocates nothing; the caller still supplies x and the output buffers.
+ *   Arguments, results and errors are those of nvfp4_quantize.
+ *   Limit: the array holds 2048 partial maxima, which is what any call needs
+ *   whatever the tensor size (the amax pass uses at most 2048 CTAs); a build
+ *   whose workspace requirement exceeded the array would get
+ *   NVFP4_ERR_WORKSPACE.
+ *   The first call on a device looks up the array's device address (and
+ *   creates the CUDA context if needed); make that first call before any
+ *   stream capture.  All calls on a device share the array and it keeps the
+ *   previous call's contents (nothing in it needs clearing): calls that can
+ *   run at the same time on the GPU, e.g. on unordered streams, race on it.
+ */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                    nvfp4_block block, nvfp4_round round, uint64_t seed,
+                                    const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
+                                    nvfp4_stream_t stream);
+
+/*
  * nvfp4_rht_quantize -- the Wgrad operand path (paper page, limitations
  * paragraph: Hadamard only on Wgrad; blog: Hadamard transforms reshape the
  * distribution).  Every run of 16 consecutive rows (tokens) of each column

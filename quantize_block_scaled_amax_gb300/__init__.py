@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
-    "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_quantize_noalloc", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_workspace_size.argtypes = []
             L.nvfp4_quantize.restype = st
             L.nvfp4_quantize.argtypes = [vp, st, i64, i64, i64, st, st, u64, tp, tp, vp, ctypes.c_size_t, vp]
+            L.nvfp4_quantize_noalloc.restype = st
+            L.nvfp4_quantize_noalloc.argtypes = [vp, st, i64, i64, i64, st, st, u64, tp, tp, vp]
             L.nvfp4_rht_quantize.restype = st
             L.nvfp4_rht_quantize.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t, vp]
             L.nvfp4_gemm.restype = st
@@ -192,6 +194,27 @@ def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", see
                               seed, ctypes.byref(r) if r is not None else None,
                               ctypes.byref(c) if c is not None else None, ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "nvfp4_quantize")
+    return (out_rowwise if rowwise else None), (out_colwise if colwise else None)
+
+
+def nvfp4_quantize_noalloc(x: torch.Tensor, block: str = "1x16", round: str = "rtn", seed: int = 0, *,
+                           rowwise: bool = True, colwise: bool = False, scale_layout: str = "mma",
+                           out_rowwise: QTensor | None = None, out_colwise: QTensor | None = None, stream=None):
+    """nvfp4_quantize without a workspace: for callers that cannot allocate
+    device memory, the library keeps the amax scratch in a fixed device array
+    of its own.  Pass preallocated outputs to allocate nothing here either."""
+    _check_input(x)
+    rows, cols = x.shape
+    if rowwise and out_rowwise is None:
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout)
+    if colwise and out_colwise is None:
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+    r = out_rowwise.c() if rowwise else None
+    c = out_colwise.c() if colwise else None
+    st = lib().nvfp4_quantize_noalloc(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _BLOCKS[block],
+                                      _ROUNDS[round], seed, ctypes.byref(r) if r is not None else None,
+                                      ctypes.byref(c) if c is not None else None, _stream(stream))
+    _check(st, "nvfp4_quantize_noalloc")
     return (out_rowwise if rowwise else None), (out_colwise if colwise else None)
 
 

@@ -361,6 +361,66 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
     return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, NVFP4_OUT_FP32, K, nullptr, 0, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Quantize without a caller workspace.
+//
+// The amax pass of nvfp4_quantize keeps one 32-bit partial maximum per CTA
+// (at most kMaxPartials of them) in scratch memory.  nvfp4_quantize_noalloc
+// keeps that scratch in the fixed array below instead, so a caller that has
+// no way to obtain device memory can still quantize.  The array is 8 KB and
+// lives on every device that loads this library until the process exits.
+// Every call on a device uses the same array: calls whose work overlaps on
+// the GPU (different streams, no ordering between them) race on it.  Nothing
+// in it has to start at zero: each call's amax pass writes every slot that
+// the same call's encode pass reads.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kMaxPartials];
+
+namespace nvfp4 {
+namespace {
+
+void* g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the first call on a device does this).
+nvfp4_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(NVFP4_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                    nvfp4_block block, nvfp4_round round, uint64_t seed,
+                                    const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
+                                    nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    // A call never needs more partial slots than the workspace contract
+    // states; refuse if the fixed array were ever smaller than that.
+    const size_t need = nvfp4_workspace_size();
+    if (need > sizeof(g_noalloc_scratch))
+        return fail(NVFP4_ERR_WORKSPACE, "quantize needs %zu bytes of scratch, the fixed array holds %zu", need,
+                    sizeof(g_noalloc_scratch));
+    void* scratch = nullptr;
+    nvfp4_status st = noalloc_scratch(&scratch);
+    if (st) return st;
+    return nvfp4_quantize(x, dtype, rows, cols, ldx, block, round, seed, out_rowwise, out_colwise, scratch,
+                          sizeof(g_noalloc_scratch), stream);
+}
+
 nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
