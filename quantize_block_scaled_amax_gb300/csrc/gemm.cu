@@ -8,18 +8,26 @@
 // put the linear layers' Fprop/Dgrad/Wgrad on block-scaled FP4 MMA with FP32
 // accumulation; this kernel is that MMA.
 //
-// Structure (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: A/B code tiles (128 rows x 128 bytes, 128-byte
-//               swizzle) and the matching 2 KB scale atoms (bulk copies) into
-//               a ring of smem stages, one mbarrier per stage.
-//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the
-//               scale atoms to TMEM, then four
+// Tile 128 x 256 (M x N), K staged 256 at a time; one persistent CTA per SM,
+// 16 warps in four warpgroups:
+//   warp 0      TMA producer: A and B code tiles (128-byte swizzle) into a
+//               4-stage smem ring (48 KB per stage), plus B's block scales
+//               for the stage (a 16-byte x 256-row box) when K % 256 == 0.
+//   warp 1      TMEM owner and MMA issuer: four
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//               (M=128, N=128, K=64 each) accumulate into one of two TMEM
-//               accumulators; tcgen05.commit releases the stage / signals
-//               the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (thread = row),
-//               x alpha, convert, store; then release the accumulator.
+//               (M=128, N=256, K=64) per stage into one TMEM accumulator.
+//   warps 4-7   scale-factor writers, one per TMEM lane quarter: A scales
+//               come straight from the row-major scale buffer (one 16-byte
+//               load per row per stage, prefetched 3 stages ahead), B scales
+//               from the stage's smem box; both go into TMEM with
+//               tcgen05.st (layout at scale_role).  Scale copies through the
+//               tensor pipe (tcgen05.cp) would serialize with the MMAs.
+//   warps 8-15  epilogue: two warps per lane quarter drain 128 accumulator
+//               columns each with tcgen05.ld, release the accumulator, then
+//               scale by alpha, convert and store through a 2 KB swizzled
+//               smem staging tile with TMA tensor stores.
+// Registers: 128 per thread (512 threads fill the register file); the
+// epilogue holds its 128 accumulator words with a few words spilled.
 // Every mbarrier wait is bounded: past the limit the waiter records
 // NVFP4_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag and all
 // roles drain out to the final barrier, where TMEM is freed.
@@ -35,33 +43,49 @@ namespace nvfp4 {
 namespace gemm {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
 constexpr int BK = 256;            // K elements per stage
 constexpr int BKB = BK / 2;        // bytes per row per stage (= 128, the swizzle width)
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kMmaK = 64;          // K per tcgen05.mma (FP4)
 constexpr int kMmaPerStage = BK / kMmaK;
 constexpr int kATileBytes = BM * BKB;      // 16 KB
-constexpr int kBTileBytes = BN * BKB;      // 16 KB
-constexpr int kSfTileBytes = 128 * BK / 16; // 2 KB: 128 rows x 16 scales
-constexpr int kStageBytes = kATileBytes + kBTileBytes + 2 * kSfTileBytes;
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kBTileBytes = BN * BKB;      // 32 KB
+constexpr int kSfbTileBytes = BN * 16;     // 4 KB: 256 rows x 16 scales
+constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfbTileBytes;
+constexpr int kThreads = 512;
+constexpr int kEpiWarps = 8;
+constexpr int kSfWarps = 4;
+constexpr int kStagingBytes = 32 * 64;     // per epilogue warp: 32 rows x 64 bytes
+constexpr int kSfaAhead = 3;               // stages of A scales prefetched in registers
+#ifndef NVFP4_GEMM_CLUSTER
+#define NVFP4_GEMM_CLUSTER 1
+#endif
+constexpr int kCluster = NVFP4_GEMM_CLUSTER;  // CTAs sharing one B tile (multicast)
+constexpr int kBSlice = BN / kCluster;       // B rows each CTA of a cluster loads
+static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster size");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns per buffer
-constexpr uint32_t kSfColsPerStage = 2 * kMmaPerStage * 4;  // SFA + SFB, 4 columns per MMA each
-constexpr uint64_t kTimeoutNs = 4000000000ull;               // 4 s per wait
+constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns
+constexpr uint32_t kSfaCols = kMmaPerStage * 4;         // 4 columns per MMA
+constexpr uint32_t kSfbCols = kMmaPerStage * 8;         // N = 256: two 128-row groups per MMA
+constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
+constexpr uint64_t kTimeoutNs = 4000000000ull;          // 4 s per wait
+static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 struct __align__(8) SharedState {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t full[kStages];     // A/B tiles landed (TMA transaction count)
+    uint64_t sfb_full[kStages]; // B scales of the stage landed (TMA transaction count)
+    uint64_t sf_full[kStages];  // scales written to TMEM (4 scale warps)
+    uint64_t empty[kStages];    // MMAs of the stage done (tcgen05.commit)
+    uint64_t acc_full;          // accumulator complete (tcgen05.commit)
+    uint64_t acc_empty;         // accumulator drained (8 epilogue warps)
     uint32_t tmem_base;
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + sizeof(SharedState);
+constexpr size_t kSmemBytes =
+    1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kStagingBytes + sizeof(SharedState);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // ---- PTX wrappers ----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -126,14 +150,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -173,11 +189,29 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// A bounded wait taken by every lane of a warp, returning the warp's verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, SharedState* ss, uint32_t* status) {
+    const bool ok = mbar_wait(bar, parity, ss, status);
+    __syncwarp();
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -187,7 +221,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -195,49 +228,333 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 16 block scales (one stage: 256 K elements) of one row from the row-major
+// scale buffer; blocks at or past nkb read as 0.  vec: 16-byte aligned rows.
+__device__ __forceinline__ uint4 load_row_scales(const uint8_t* row, int kt, int nkb, bool vec) {
+    const int b0 = 16 * kt;
+    if (vec && b0 + 16 <= nkb) return __ldg(reinterpret_cast<const uint4*>(row + b0));
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + b0);
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (b0 + 4 <= nkb) r.x = __ldg(w);
+    if (b0 + 8 <= nkb) r.y = __ldg(w + 1);
+    if (b0 + 12 <= nkb) r.z = __ldg(w + 2);
+    if (b0 + 16 <= nkb) r.w = __ldg(w + 3);
+    return r;
+}
+
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ int cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+
 // ---- the kernel ----------------------------------------------------------------
 struct Params {
-    const uint8_t* a_scales;
-    const uint8_t* b_scales;
+    const uint8_t* a_scales;  // [M][K/16] row-major E4M3
+    const uint8_t* b_scales;  // [N][K/16]
     const float* a_amax;
     const float* b_amax;
-    void* c;
-    int64_t ldc;
     int M, N, K;
     int num_m, num_n, num_k;  // tiles
-    int n_katoms;             // scale atoms per 128-row group
+    int nkb;                  // K / 16
+    int sf_vec;               // rows of the scale buffers are 16-byte aligned (B scales come by TMA)
     int out_fp32;
     uint32_t* status;
 };
 
+// Tile schedule: a cluster of kCluster CTAs takes kCluster consecutive M
+// tiles of one N tile (its "group"); clusters walk the groups with M fastest.
+// Every CTA of a cluster visits the same groups in the same order.  A CTA
+// whose M tile lies past the matrix still runs (its A rows read as zero and
+// its stores fall outside C), because its share of the B tile feeds the
+// other CTAs.
+struct Sched {
+    int rank, cid, nclusters, num_mg, num_groups;
+    __device__ explicit Sched(const Params& p) {
+        rank = kCluster > 1 ? cluster_rank() : 0;
+        cid = (int)blockIdx.x / kCluster;
+        nclusters = (int)gridDim.x / kCluster;
+        num_mg = (p.num_m + kCluster - 1) / kCluster;
+        num_groups = num_mg * p.num_n;
+    }
+    __device__ int count() const { return cid < num_groups ? (num_groups - cid + nclusters - 1) / nclusters : 0; }
+    __device__ void tile(int i, int& mb, int& nb) const {
+        const int g = cid + i * nclusters;
+        nb = g / num_mg;
+        mb = (g % num_mg) * kCluster + rank;
+    }
+};
+
+__device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
+                                              const CUtensorMap* tmap_sfb, const Params& p, SharedState* ss, uint8_t* sA,
+                                              uint8_t* sB, uint8_t* sSfb) {
+    const Sched S(p);
+    const uint16_t mask = (uint16_t)((1u << kCluster) - 1u);
+    uint32_t it = 0;
+    for (int i = 0; i < S.count(); ++i) {
+        int mb, nb;
+        S.tile(i, mb, nb);
+        for (int kt = 0; kt < p.num_k; ++kt, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1u;
+            // free in every CTA of the cluster: the multicasts below write all of them
+            if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+            const int rb = nb * BN + S.rank * kBSlice;
+            if (p.sf_vec) {
+                // the small scale box first: the scale writers need only it
+                mbar_arrive_expect_tx(&ss->sfb_full[s], kSfbTileBytes);
+                uint8_t* dst = sSfb + s * kSfbTileBytes + S.rank * kBSlice * 16;
+                if (kCluster > 1) tma_load_2d_mc(dst, tmap_sfb, &ss->sfb_full[s], kt * 16, rb, mask);
+                else tma_load_2d(dst, tmap_sfb, &ss->sfb_full[s], kt * 16, rb);
+            }
+            mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
+            tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kt * BKB, mb * BM);
+            uint8_t* bdst = sB + s * kBTileBytes + S.rank * kBSlice * BKB;
+            if (kCluster > 1) tma_load_2d_mc(bdst, tmap_b, &ss->full[s], kt * BKB, rb, mask);
+            else tma_load_2d(bdst, tmap_b, &ss->full[s], kt * BKB, rb);
+        }
+    }
+}
+
+__device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
+                                         uint32_t tmem_base) {
+    const Sched S(p);
+    const uint16_t mask = (uint16_t)((1u << kCluster) - 1u);
+    const uint32_t idesc = instr_desc_nvf4(BM, BN);
+    const uint32_t sf_base = tmem_base + kAccCols;
+    uint32_t it = 0, tc = 0;
+    for (int i = 0; i < S.count(); ++i, ++tc) {
+        if (!mbar_wait(&ss->acc_empty, (tc & 1u) ^ 1u, ss, p.status)) return;
+        tc_fence_after();
+        for (int kt = 0; kt < p.num_k; ++kt, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1u;
+            if (!mbar_wait(&ss->full[s], ph, ss, p.status) || !mbar_wait(&ss->sf_full[s], ph, ss, p.status)) return;
+            tc_fence_after();
+            const uint32_t sfa_t = sf_base + s * kSfColsPerStage;
+            const uint32_t sfb_t = sfa_t + kSfaCols;
+            const uint32_t a_s = smem_u32(sA + s * kATileBytes);
+            const uint32_t b_s = smem_u32(sB + s * kBTileBytes);
+#pragma unroll
+            for (int j = 0; j < kMmaPerStage; ++j) {
+                const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
+                const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
+                mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+            }
+            // the stage is free once every CTA of the cluster is done with it
+            if (kCluster > 1) mma_commit_mc(&ss->empty[s], mask);
+            else mma_commit(&ss->empty[s]);
+        }
+        mma_commit(&ss->acc_full);
+    }
+}
+
+// Scale-factor TMEM layout read by one MMA (measured on the hardware):
+//   A (128 rows): row r at lane r, column base + r/32 -- each lane quarter
+//     reads only its own rows, so lane r holds only its own row's word;
+//   B (256 rows): every lane quarter reads all of B: row n at lane
+//     32q + n%32, column base + n/32, the same in all four quarters.
+// Writer warp q (lanes 32q .. 32q+31 of TMEM), lane l: A row 32q + l, and B
+// rows 32c + l for c = 0..7.  Per stage, MMA j reads A words at columns
+// 4j..4j+3 (the lane's word is written into all four) and B words at
+// 8j..8j+7.
+__device__ __forceinline__ uint4 stage_a_scales(const Params& p, int it, int q, int lane) {
+    const Sched S(p);
+    const int i = it / p.num_k, kt = it % p.num_k;
+    if (i >= S.count()) return make_uint4(0u, 0u, 0u, 0u);
+    int mb, nb;
+    S.tile(i, mb, nb);
+    const int ra = mb * BM + 32 * q + lane;
+    if (ra >= p.M) return make_uint4(0u, 0u, 0u, 0u);
+    return load_row_scales(p.a_scales + (size_t)ra * p.nkb, kt, p.nkb, p.sf_vec);
+}
+
+__device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, const uint8_t* sSfb, uint32_t tmem_base,
+                                           int q, int lane) {
+    const Sched S(p);
+    const int total = S.count() * p.num_k;
+    const uint32_t sf_base = tmem_base + kAccCols;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    // A scales run kSfaAhead stages ahead in registers to hide the L2 latency
+    uint4 a0 = stage_a_scales(p, 0, q, lane), a1 = stage_a_scales(p, 1, q, lane), a2 = stage_a_scales(p, 2, q, lane);
+    for (int it = 0; it < total; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        const uint4 wa = a0;
+        a0 = a1;
+        a1 = a2;
+        a2 = stage_a_scales(p, it + kSfaAhead, q, lane);
+        uint4 wb[8];
+        if (p.sf_vec) {
+            // the B scales of this stage arrive with the code tiles
+            if (!warp_wait(&ss->sfb_full[s], ph, ss, p.status)) return;
+            const uint8_t* rows = sSfb + s * kSfbTileBytes + lane * 16;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) wb[c] = *reinterpret_cast<const uint4*>(rows + 32 * 16 * c);
+        } else {
+            int mb, nb;
+            S.tile(it / p.num_k, mb, nb);
+            const int kt = it % p.num_k;
+            const int rb = nb * BN + lane;
+            const uint8_t* pb = p.b_scales + (size_t)rb * p.nkb;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                wb[c] = rb + 32 * c < p.N ? load_row_scales(pb + (size_t)32 * c * p.nkb, kt, p.nkb, false)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!warp_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+        tc_fence_after();
+        const uint32_t col = lane_addr + sf_base + s * kSfColsPerStage;
+        const uint32_t va[16] = {wa.x, wa.x, wa.x, wa.x, wa.y, wa.y, wa.y, wa.y,
+                                 wa.z, wa.z, wa.z, wa.z, wa.w, wa.w, wa.w, wa.w};
+        tmem_st_x16(col, va);
+        uint32_t vb[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            vb[c] = wb[c].x;
+            vb[8 + c] = wb[c].y;
+        }
+        tmem_st_x16(col + kSfaCols, vb);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            vb[c] = wb[c].z;
+            vb[8 + c] = wb[c].w;
+        }
+        tmem_st_x16(col + kSfaCols + 16, vb);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ss->sf_full[s]);
+    }
+}
+
+// Epilogue warp e: lane quarter q = warp % 4, accumulator half h (columns
+// [128h, 128h + 128)).  Rows leave through a 32 x 64-byte staging tile in
+// the 64-byte swizzle (16-byte chunk j of row r at position j ^ ((r/2) % 4)),
+// one TMA store per 64 bytes of every row.
+__device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
+                                              uint8_t* stage, uint32_t tmem_base, int q, int h, int lane) {
+    const Sched S(p);
+    const float alpha = __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
+    const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
+    uint8_t* row_base = stage + lane * 64;
+    const int sw = (lane >> 1) & 3;
+    uint32_t tc = 0;
+    for (int i = 0; i < S.count(); ++i, ++tc) {
+        int mb, nb;
+        S.tile(i, mb, nb);
+        if (!warp_wait(&ss->acc_full, tc & 1u, ss, p.status)) break;
+        tc_fence_after();
+        uint32_t acc[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, acc + 32 * c);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ss->acc_empty);
+
+        const int y = mb * BM + 32 * q;
+        const int col0 = nb * BN + 128 * h;
+        if (p.out_fp32) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16 floats per 64-byte row
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t* a = acc + 16 * c + 4 * j;
+                    const uint4 v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
+                                               __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
+                                               __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
+                                               __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
+                    *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && y < p.M && col0 + 16 * c < p.N) {
+                    tma_store_2d(tmap_c, stage, col0 + 16 * c, y);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {  // 32 bf16 per 64-byte row
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t* a = acc + 32 * c + 8 * j;
+                    const uint4 v = make_uint4(
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
+                    *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && y < p.M && col0 + 32 * c < p.N) {
+                    tma_store_2d(tmap_c, stage, col0 + 32 * c, y);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+            }
+        }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sfb,
                      const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + kStages * kATileBytes;
-    uint8_t* sSFA = sB + kStages * kBTileBytes;
-    uint8_t* sSFB = sSFA + kStages * kSfTileBytes;
-    SharedState* ss = reinterpret_cast<SharedState*>(sSFB + kStages * kSfTileBytes);
+    uint8_t* sSfb = sB + kStages * kBTileBytes;
+    uint8_t* sStage = sSfb + kStages * kSfbTileBytes;
+    SharedState* ss = reinterpret_cast<SharedState*>(sStage + kEpiWarps * kStagingBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_tiles = p.num_m * p.num_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ss->full[s], 1);
-            mbar_init(&ss->empty[s], 1);
+            mbar_init(&ss->sfb_full[s], 1);
+            mbar_init(&ss->sf_full[s], kSfWarps);
+            mbar_init(&ss->empty[s], kCluster);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&ss->acc_full[a], 1);
-            mbar_init(&ss->acc_empty[a], kEpiWarps);
-        }
+        mbar_init(&ss->acc_full, 1);
+        mbar_init(&ss->acc_empty, kEpiWarps);
         ss->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_c) : "memory");
+        if (p.sf_vec) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_sfb) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -247,143 +564,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (kCluster > 1) cluster_sync();  // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = ss->tmem_base;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const int mb = tile % p.num_m, nb = tile / p.num_m;
-                const uint8_t* sfa_src = p.a_scales + (size_t)mb * p.n_katoms * 512;
-                const uint8_t* sfb_src = p.b_scales + (size_t)nb * p.n_katoms * 512;
-                bool ok = true;
-                for (int kt = 0; kt < p.num_k; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&ss->full[s], kStageBytes);
-                    tma_load_2d(sA + s * kATileBytes, &tmap_a, &ss->full[s], kt * BKB, mb * BM);
-                    tma_load_2d(sB + s * kBTileBytes, &tmap_b, &ss->full[s], kt * BKB, nb * BN);
-                    bulk_load(sSFA + s * kSfTileBytes, sfa_src + (size_t)kt * kSfTileBytes, kSfTileBytes,
-                              &ss->full[s]);
-                    bulk_load(sSFB + s * kSfTileBytes, sfb_src + (size_t)kt * kSfTileBytes, kSfTileBytes,
-                              &ss->full[s]);
-                }
-                if (!ok) break;
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            const uint32_t idesc = instr_desc_nvf4(BM, BN);
-            const uint32_t sf_base = tmem_base + 2 * kAccCols;
-            uint32_t it = 0;
-            uint32_t tc = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
-                const uint32_t a = tc & 1u;
-                const uint32_t aph = (tc >> 1) & 1u;
-                if (!mbar_wait(&ss->acc_empty[a], aph ^ 1u, ss, p.status)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + a * kAccCols;
-                bool ok = true;
-                for (int kt = 0; kt < p.num_k; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(&ss->full[s], ph, ss, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sfa_t = sf_base + s * kSfColsPerStage;
-                    const uint32_t sfb_t = sfa_t + kMmaPerStage * 4;
-                    const uint32_t sfa_s = smem_u32(sSFA + s * kSfTileBytes);
-                    const uint32_t sfb_s = smem_u32(sSFB + s * kSfTileBytes);
-#pragma unroll
-                    for (int j = 0; j < kMmaPerStage; ++j) {
-                        tmem_cp_32x128b_x4(sfa_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
-                        tmem_cp_32x128b_x4(sfb_t + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-                    }
-                    const uint32_t a_s = smem_u32(sA + s * kATileBytes);
-                    const uint32_t b_s = smem_u32(sB + s * kBTileBytes);
-#pragma unroll
-                    for (int j = 0; j < kMmaPerStage; ++j) {
-                        const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
-                        const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
-                        mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j,
-                                 (kt > 0 || j > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&ss->empty[s]);
-                }
-                if (!ok) break;
-                mma_commit(&ss->acc_full[a]);
-            }
+    if (warp < 8) {
+        if (warp == 0) {
+            if (lane == 0) producer_role(&tmap_a, &tmap_b, &tmap_sfb, p, ss, sA, sB, sSfb);
+        } else if (warp == 1) {
+            if (lane == 0) mma_role(p, ss, sA, sB, tmem_base);
+        } else if (warp >= 4) {
+            scale_role(p, ss, sSfb, tmem_base, warp & 3, lane);
         }
     } else {
-        // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const float alpha = __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
-        uint32_t tc = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
-            const int mb = tile % p.num_m, nb = tile / p.num_m;
-            const uint32_t a = tc & 1u;
-            const uint32_t aph = (tc >> 1) & 1u;
-            const bool ok = mbar_wait(&ss->acc_full[a], aph, ss, p.status);
-            __syncwarp();
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            tc_fence_after();
-            const int row = mb * BM + q * 32 + lane;
-            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + a * kAccCols;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + ch * 32, r);
-                const int col0 = nb * BN + ch * 32;
-                if (row < p.M) {
-                    if (p.out_fp32) {
-                        float* dst = static_cast<float*>(p.c) + (int64_t)row * p.ldc + col0;
-                        if (col0 + 32 <= p.N) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(dst + j) =
-                                    make_float4(__fmul_rn(__uint_as_float(r[j]), alpha),
-                                                __fmul_rn(__uint_as_float(r[j + 1]), alpha),
-                                                __fmul_rn(__uint_as_float(r[j + 2]), alpha),
-                                                __fmul_rn(__uint_as_float(r[j + 3]), alpha));
-                        } else {
-                            for (int j = 0; j < 32 && col0 + j < p.N; ++j)
-                                dst[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
-                        }
-                    } else {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + (int64_t)row * p.ldc + col0;
-                        if (col0 + 32 <= p.N) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[j]), alpha),
-                                                  __fmul_rn(__uint_as_float(r[j + 1]), alpha));
-                                v.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[j + 2]), alpha),
-                                                  __fmul_rn(__uint_as_float(r[j + 3]), alpha));
-                                v.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[j + 4]), alpha),
-                                                  __fmul_rn(__uint_as_float(r[j + 5]), alpha));
-                                v.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[j + 6]), alpha),
-                                                  __fmul_rn(__uint_as_float(r[j + 7]), alpha));
-                                *reinterpret_cast<uint4*>(dst + j) = v;
-                            }
-                        } else {
-                            for (int j = 0; j < 32 && col0 + j < p.N; ++j)
-                                dst[j] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[j]), alpha));
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ss->acc_empty[a]);
-        }
+        const int e = warp - 8;
+        epilogue_role(&tmap_c, p, ss, sStage + e * kStagingBytes, tmem_base, warp & 3, e >> 2, lane);
     }
 
-    // Drain: every role reaches this barrier, then warp 1 frees TMEM.
+    // Drain: every role reaches this barrier (every CTA of the cluster: no
+    // peer may still multicast into this CTA), then warp 1 frees TMEM.
     tc_fence_before();
     __syncthreads();
+    if (kCluster > 1) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
@@ -411,16 +613,17 @@ int get_encoder(const char** msg) {
     return 0;
 }
 
-// 2D tensor map over a [rows][row_bytes] byte matrix with row stride ld,
-// box 128 x 128 bytes, 128-byte swizzle, zero fill outside the matrix.
-int make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int64_t ld, const char** msg) {
-    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {(cuuint32_t)BKB, (cuuint32_t)BM};
+// 2D tensor map over a [rows][row_elems] matrix with row stride ld_bytes:
+// box box_x x box_y elements, zero fill outside.
+int make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int64_t rows, int64_t row_elems,
+             int64_t ld_bytes, int box_x, int box_y, CUtensorMapSwizzle swizzle, const char** msg) {
+    cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_y};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *msg = "cuTensorMapEncodeTiled failed";
         return 1;
@@ -429,6 +632,7 @@ int make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_
 }
 
 bool g_attr_set[64] = {};
+int g_max_clusters[64] = {};
 std::mutex g_attr_mu;
 
 }  // namespace gemm
@@ -440,9 +644,33 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
         *msg = "dimension exceeds 2^31";
         return -1;
     }
-    CUtensorMap ta, tb;
-    if (make_code_map(&ta, g.a_codes, g.M, g.K / 2, g.lda, msg)) return 1;
-    if (make_code_map(&tb, g.b_codes, g.N, g.K / 2, g.ldb, msg)) return 1;
+    CUtensorMap ta, tb, tcm, tsf;
+    if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.M, g.K / 2, g.lda, BKB, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B, msg))
+        return 1;
+    if (make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, kBSlice,
+                 CU_TENSOR_MAP_SWIZZLE_128B, msg))
+        return 1;
+    if (g.out_fp32) {
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.c, g.M, g.N, g.ldc * 4, 16, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B, msg))
+            return 1;
+    } else {
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B, msg))
+            return 1;
+    }
+    const int nkb = (int)(g.K / 16);
+    const bool sf_vec = (nkb % 16 == 0) &&
+                        ((reinterpret_cast<uintptr_t>(g.a_scales) | reinterpret_cast<uintptr_t>(g.b_scales)) % 16 == 0);
+    if (sf_vec) {
+        // B scales, [N][K/16] bytes: a 16-byte x kBSlice-row box per CTA per stage
+        if (make_map(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_scales, g.N, nkb, nkb, 16, kBSlice,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, msg))
+            return 1;
+    } else {
+        tsf = ta;  // unused
+    }
     {
         int dev = 0;
         cudaGetDevice(&dev);
@@ -459,20 +687,50 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.b_scales = g.b_scales;
     p.a_amax = g.a_amax;
     p.b_amax = g.b_amax;
-    p.c = g.c;
-    p.ldc = g.ldc;
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
     p.num_m = (int)((g.M + BM - 1) / BM);
     p.num_n = (int)((g.N + BN - 1) / BN);
     p.num_k = (int)((g.K + BK - 1) / BK);
-    p.n_katoms = (int)(4 * ((g.K + 255) / 256));
+    p.nkb = nkb;
+    p.sf_vec = sf_vec ? 1 : 0;
     p.out_fp32 = g.out_fp32;
     p.status = g.status;
-    const int tiles = p.num_m * p.num_n;
-    const int grid = tiles < g.num_sms ? tiles : g.num_sms;
-    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: as many clusters as fit at once, at most one per tile group
+    int max_clusters = 0;
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if (dev >= 0 && dev < 64 && g_max_clusters[dev] == 0) {
+            cfg.gridDim = dim3((unsigned)(g.num_sms / kCluster * kCluster));
+            int n = 0;
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_kernel, &cfg);
+            if (e != cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();
+                n = g.num_sms / kCluster;
+            }
+            g_max_clusters[dev] = n;
+        }
+        max_clusters = (dev >= 0 && dev < 64) ? g_max_clusters[dev] : g.num_sms / kCluster;
+    }
+    const int groups = ((p.num_m + kCluster - 1) / kCluster) * p.num_n;
+    const int clusters = groups < max_clusters ? groups : max_clusters;
+    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel, ta, tb, tcm, tsf, p);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 
