@@ -132,11 +132,12 @@ nvfp4_status check_workspace(void* ws, size_t bytes) {
     return NVFP4_OK;
 }
 
-int amax_grid(int64_t rows, int64_t cols, int num_sms) {
-    // ~4 vectors of 16 bytes per thread per pass at most; at least one CTA
-    const int64_t vec = rows * cols / 8;
-    int64_t g = ceil_div(vec, (int64_t)kAmaxThreads * 4);
-    g = std::min<int64_t>(g, (int64_t)num_sms * 4);
+int amax_grid(int64_t rows, int64_t cols, int64_t ldx, bool fp32, int num_sms) {
+    // dense: one CTA per chunk of kAmaxThreads * kAmaxUnroll vectors, up to 8
+    // CTAs per SM; strided: CTAs walk rows
+    const int64_t units = ldx == cols ? ceil_div(rows * cols / (fp32 ? 4 : 8), (int64_t)kAmaxThreads * kAmaxUnroll)
+                                      : rows;
+    int64_t g = std::min<int64_t>(units, (int64_t)num_sms * 8);
     g = std::min<int64_t>(g, kMaxPartials);
     return (int)std::max<int64_t>(g, 1);
 }
@@ -204,7 +205,7 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
     if (out_rowwise && (st = zero_scale_padding(out_rowwise, s))) return st;
     if (out_colwise && (st = zero_scale_padding(out_colwise, s))) return st;
 
-    const int ag = amax_grid(rows, cols, dev->num_sms);
+    const int ag = amax_grid(rows, cols, ldx, fp32, dev->num_sms);
     launch_amax(x, fp32, rows, cols, ldx, partials, ag, s);
     if ((st = check_launch("amax"))) return st;
 
@@ -219,8 +220,8 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
         return check_launch("quantize_2d");
     }
     if (out_rowwise) {
-        const int64_t groups = rows * ceil_div(cols, 64);
-        const int g = cap_grid(ceil_div(groups, kQuantThreads), 8, dev->num_sms);
+        const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
+        const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
         launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
                                 scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, seed, g, s);
         if ((st = check_launch("quantize_rowwise"))) return st;
@@ -254,7 +255,7 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     if ((st = zero_scale_padding(out_colwise, s))) return st;
     const int64_t units = (rows / 16) * (cols / (fp32 ? 4 : 8));
     const int ag = (int)std::max<int64_t>(
-        1, std::min<int64_t>({ceil_div(units, kAmaxThreads), (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
+        1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads), (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
     launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
     if ((st = check_launch("rht_amax"))) return st;
     const int g = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);

@@ -74,13 +74,13 @@ __device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc) {
 }
 
 // ---------------------------------------------------------------------------
-// E2M1 round to nearest (ties to even), saturating, two at a time.  The
-// hardware conversion places its first source operand in the high nibble,
-// so element 2j (low nibble) is the second operand.  Each 8-bit result is
-// widened on its own (cvt.u32.u8) before packing: packing four 8-bit
-// registers with one vector mov produced wrong bytes inside the 16x16
-// kernel with this toolchain.  The sign bit of each input is OR-ed in so
-// that negative values rounding to 0 keep code 0x8.
+// E2M1 codes of values, two at a time: the hardware conversion rounds to
+// nearest (ties to even) and saturates to +-6; it keeps the sign of a value
+// that rounds to zero (code 0x8 for -0).  It places its first source operand
+// in the high nibble, so element 2j (low nibble) is the second operand.  Each
+// 8-bit result is widened on its own (cvt.u32.u8) before packing: packing four
+// 8-bit registers with one vector mov produced wrong bytes inside the 16x16
+// kernel with this toolchain.
 __device__ __forceinline__ uint32_t e2m1x2_rtn(float lo, float hi) {
     uint32_t h;
     asm volatile(
@@ -96,27 +96,35 @@ __device__ __forceinline__ uint32_t e2m1x8_rtn(const float v[8]) {
     uint32_t out = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) out |= e2m1x2_rtn(v[2 * j], v[2 * j + 1]) << (8 * j);
-    uint32_t signs = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) signs |= (__float_as_uint(v[j]) >> 31) << (4 * j + 3);
-    return out | signs;
+    return out;
 }
 
-// E2M1 stochastic rounding of one value with its 32-bit random word: the
-// magnitude (saturated at 6) goes up to the next grid point iff
-// (rbits >> 8) * 2^-24 < frac, frac = (|v| - lo) / (hi - lo) (exact).
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t rbits) {
-    uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    float a = fminf(fabsf(v), 6.0f);
-    // scale the binade so the grid spacing becomes 1: [0,2) x2, [2,4) x1, [4,6] x0.5
-    float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-    float t = __fmul_rn(a, s);
-    float k = floorf(t);
-    float frac = __fsub_rn(t, k);
-    uint32_t code_lo = a < 2.0f ? (uint32_t)k : (a < 4.0f ? (uint32_t)k + 2u : 6u);
-    uint32_t up = ((float)(rbits >> 8) < __fmul_rn(frac, 16777216.0f)) ? 1u : 0u;
-    uint32_t code = a >= 6.0f ? 7u : code_lo + up;
-    return sign | code;
+// E2M1 stochastic rounding of one value v with its 32-bit random word w, as
+// the grid value it rounds to (sign kept).  The contract: with a = min(|v|, 6),
+// lo <= a < hi the neighbouring grid points, frac = (a - lo) / (hi - lo) and
+// u = w >> 8, a goes up to hi iff u * 2^-24 < frac.
+//
+// Computed with directed rounding instead of a compare.  Let s = hi - lo be
+// the grid spacing of a's binade (0.5 below 2, otherwise half the binade's
+// power of two) and t = u * 2^-24.  Then lo + s * ceil(frac - t) is hi exactly
+// when frac > t, and ceil(frac - t) = ceil(a/s - t) - lo/s, so the rounded
+// value is s * ceil((a - s t) / s).  a - s t is formed by one FMA rounded
+// upward (s t is exact: a power of two times a 24-bit integer), and rounding
+// upward never moves a value past the next multiple of s (those are
+// representable), so the ceiling is unchanged; adding M = 1.5 * 2^23 * s,
+// whose binade has spacing s, rounded upward again, lands on M + that
+// multiple, and subtracting M is exact.  For |v| > 6 the result is >= 6 and
+// the saturating conversion gives code 7, which is what clamping to 6 first
+// gives; so no clamp is needed (|v| stays finite: |v| <= ~12 by construction
+// of the block scale).
+__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t w) {
+    // p = 2^max(e, 0) for |v| in [2^e, 2^(e+1)); s = p / 2
+    const float p = fmaxf(__uint_as_float(__float_as_uint(v) & 0x7F800000u), 1.0f);
+    const float uf = __uint2float_rn(w & 0xFFFFFF00u);  // u * 2^8, exact
+    const float z = __fmaf_ru(uf, __fmul_rn(p, -1.16415321826934814453125e-10f /* -2^-33 */), fabsf(v));
+    const float m = __fmul_rn(p, 6291456.0f);  // 1.5 * 2^22 * p = 1.5 * 2^23 * s
+    const float y = __fsub_rn(__fadd_ru(z, m), m);
+    return __uint_as_float(__float_as_uint(y) | (__float_as_uint(v) & 0x80000000u));
 }
 
 // ---------------------------------------------------------------------------
@@ -124,9 +132,9 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t rbits) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        const uint64_t p0 = 0xD2511F53ull * c.x;  // one 32x32 -> 64-bit multiply each
+        const uint64_t p1 = 0xCD9E8D57ull * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
@@ -150,17 +158,17 @@ __device__ __forceinline__ uint2 encode16(const float v[16], uint64_t seed, uint
         out.x = e2m1x8_rtn(v);
         out.y = e2m1x8_rtn(v + 8);
     } else {
-        uint32_t w[2] = {0u, 0u};
+        float y[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint4 r = sr_words(seed, i0 + 4 * q);
-            uint32_t c0 = e2m1_sr(v[4 * q + 0], r.x), c1 = e2m1_sr(v[4 * q + 1], r.y);
-            uint32_t c2 = e2m1_sr(v[4 * q + 2], r.z), c3 = e2m1_sr(v[4 * q + 3], r.w);
-            uint32_t nib = c0 | (c1 << 4) | (c2 << 8) | (c3 << 12);
-            w[q >> 1] |= nib << (16 * (q & 1));
+            const uint4 r = sr_words(seed, i0 + 4 * q);
+            y[4 * q + 0] = e2m1_sr_value(v[4 * q + 0], r.x);
+            y[4 * q + 1] = e2m1_sr_value(v[4 * q + 1], r.y);
+            y[4 * q + 2] = e2m1_sr_value(v[4 * q + 2], r.z);
+            y[4 * q + 3] = e2m1_sr_value(v[4 * q + 3], r.w);
         }
-        out.x = w[0];
-        out.y = w[1];
+        out.x = e2m1x8_rtn(y);  // exact: every y is a grid value
+        out.y = e2m1x8_rtn(y + 8);
     }
     return out;
 }

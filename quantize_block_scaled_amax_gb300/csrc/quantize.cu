@@ -87,7 +87,10 @@ __device__ __forceinline__ float vec_elem<float>(const uint4& u, int c) {
 
 // ---------------------------------------------------------------------------
 // Pass 1: tensor amax (as FP32 magnitude bit patterns; a NaN or an infinity
-// gives a pattern >= 0x7f800000).
+// gives a pattern >= 0x7f800000).  A dense input is cut into chunks of
+// kAmaxThreads * kAmaxUnroll 16-byte vectors; a CTA reads whole chunks (every
+// thread issues its kAmaxUnroll loads before using any) and walks the chunks
+// with a grid stride, so each CTA streams long contiguous runs.
 template <typename T>
 __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
                                                             int64_t ldx, uint32_t* __restrict__ partials) {
@@ -97,15 +100,19 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const T* __restrict_
     if (ldx == cols) {
         const uint4* p = reinterpret_cast<const uint4*>(x);
         const int64_t nvec = rows * cols / V;
-        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        for (; i + 3 * stride < nvec; i += 4 * stride) {
-            uint4 a = __ldg(p + i), b = __ldg(p + i + stride);
-            uint4 c = __ldg(p + i + 2 * stride), d = __ldg(p + i + 3 * stride);
-            m = max(m, max(max(vec_absmax_bits<T>(a), vec_absmax_bits<T>(b)),
-                           max(vec_absmax_bits<T>(c), vec_absmax_bits<T>(d))));
+        constexpr int64_t kChunk = (int64_t)kAmaxThreads * kAmaxUnroll;
+        const int64_t nchunks = nvec / kChunk;
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            const uint4* q = p + c * kChunk + threadIdx.x;
+            uint4 v[kAmaxUnroll];
+#pragma unroll
+            for (int k = 0; k < kAmaxUnroll; ++k) v[k] = __ldg(q + k * kAmaxThreads);
+#pragma unroll
+            for (int k = 0; k < kAmaxUnroll; ++k) m = max(m, vec_absmax_bits<T>(v[k]));
         }
-        for (; i < nvec; i += stride) m = max(m, vec_absmax_bits<T>(__ldg(p + i)));
+        for (int64_t i = nchunks * kChunk + (int64_t)blockIdx.x * kAmaxThreads + threadIdx.x; i < nvec;
+             i += (int64_t)gridDim.x * kAmaxThreads)
+            m = max(m, vec_absmax_bits<T>(__ldg(p + i)));
     } else {
         const int64_t vpr = cols / V;
         for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const T* __restrict_
 // consecutive rows x one 16-byte column vector (8 bf16 or 4 fp32 columns);
 // every column of the unit is one 16-point chunk.
 template <typename T>
-__global__ void __launch_bounds__(kAmaxThreads) rht_amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+__global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
                                                                 int64_t ldx, uint64_t rht_seed,
                                                                 uint32_t* __restrict__ partials) {
     __shared__ uint32_t red[33];
@@ -169,60 +176,74 @@ __device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales&
 }
 
 // ---------------------------------------------------------------------------
-// Pass 2, rowwise 1x16: one thread per group of 64 consecutive elements of a
-// row (4 blocks: 32 bytes of codes, 4 scale bytes).
+// One 1x16 block of T in 16-byte vectors: load, block amax, unpack to FP32.
+template <typename T>
+struct Block16 {
+    static constexpr int kVecs = 16 * sizeof(T) / 16;
+    uint4 raw[kVecs];
+    __device__ __forceinline__ void load(const T* p) {
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) raw[k] = __ldg(reinterpret_cast<const uint4*>(p) + k);
+    }
+    __device__ __forceinline__ float absmax() const {
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) m = max(m, vec_absmax_bits<T>(raw[k]));
+        return __uint_as_float(m);
+    }
+    __device__ __forceinline__ void unpack(float v[16]) const {
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k)
+#pragma unroll
+            for (int c = 0; c < 16 / kVecs; ++c) v[k * (16 / kVecs) + c] = vec_elem<T>(raw[k], c);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Pass 2, rowwise 1x16.  A warp takes 64 consecutive blocks of one row (lane l
+// blocks l and l + 32: two coalesced 1 KB runs of bf16), loads both before
+// encoding either, and writes 8 bytes of codes and one scale byte per block.
+// Warp items run in the reverse of the amax pass's order, so the part of the
+// input read last by that pass (still in L2) is read first here.
 template <typename T, bool kSR>
-__global__ void __launch_bounds__(kQuantThreads) quantize_rowwise_kernel(
+__global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantize_rowwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
     uint64_t seed) {
     __shared__ uint32_t red[33];
     const TensorScales ts = reduce_partials(partials, npartials, amax_out, status, red);
-    const int64_t gpr = (cols + 63) / 64;
-    const int64_t ngroups = rows * gpr;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < ngroups; t += stride) {
-        const int64_t g = ngroups - 1 - t;  // reverse of the amax pass order
-        const int64_t r = g / gpr;
-        const int64_t c0 = (g - r * gpr) * 64;
-        const int nb = (cols - c0) >= 64 ? 4 : (int)((cols - c0) / 16);
-        const T* src = x + r * ldx + c0;
-        uint8_t* dst = codes + r * ld_codes + c0 / 2;
-        const uint64_t i0 = (uint64_t)r * (uint64_t)cols + (uint64_t)c0;
-        uint32_t sbs = 0;
-        if (nb == 4) {
-            float v[4][16];
+    const int lane = threadIdx.x & 31;
+    const int64_t bpr = cols / 16;
+    const int64_t ipr = (bpr + kRowItemBlocks - 1) / kRowItemBlocks;
+    const int64_t nitems = rows * ipr;
+    const int64_t nwarps = (int64_t)gridDim.x * (kQuantThreads / 32);
+    for (int64_t it = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5); it < nitems; it += nwarps) {
+        const int64_t item = nitems - 1 - it;
+        const int64_t r = item / ipr;
+        const int64_t kb0 = (item - r * ipr) * kRowItemBlocks + lane;
+        Block16<T> blk[2];
+        bool ok[2];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                In<T>::load8(src + 16 * b, v[b]);
-                In<T>::load8(src + 16 * b + 8, v[b] + 8);
-            }
-            uint2 c[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                uint32_t sb;
-                c[b] = quantize_block<kSR>(v[b], ts, seed, i0 + 16 * b, sb);
-                sbs |= sb << (8 * b);
-            }
-            reinterpret_cast<uint4*>(dst)[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
-            reinterpret_cast<uint4*>(dst)[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
-        } else {
-            for (int b = 0; b < nb; ++b) {
-                float v[16];
-                In<T>::load8(src + 16 * b, v);
-                In<T>::load8(src + 16 * b + 8, v + 8);
-                uint32_t sb;
-                uint2 c = quantize_block<kSR>(v, ts, seed, i0 + 16 * b, sb);
-                reinterpret_cast<uint2*>(dst)[b] = c;
-                sbs |= sb << (8 * b);
-            }
+        for (int h = 0; h < 2; ++h) {
+            ok[h] = kb0 + 32 * h < bpr;
+            if (ok[h]) blk[h].load(x + r * ldx + (kb0 + 32 * h) * 16);
         }
-        const int64_t kb0 = c0 / 16;
-        const int64_t off = so.offset(r, kb0);
-        if (nb == 4 && (off & 3) == 0) {
-            *reinterpret_cast<uint32_t*>(so.p + off) = sbs;
-        } else {
-            for (int b = 0; b < nb; ++b) so.p[so.offset(r, kb0 + b)] = (uint8_t)(sbs >> (8 * b));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ok[h]) continue;
+            const int64_t kb = kb0 + 32 * h;
+            BlockScale bs = block_scale(blk[h].absmax(), ts.s_enc);
+            if (!ts.finite) bs.sb = 0u;
+            uint2 c = make_uint2(0u, 0u);
+            if (bs.sb != 0u) {
+                float v[16];
+                blk[h].unpack(v);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
+                c = encode16<kSR>(v, seed, (uint64_t)r * (uint64_t)cols + (uint64_t)kb * 16);
+            }
+            *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
+            so.p[so.offset(r, kb)] = (uint8_t)bs.sb;
         }
     }
 }
@@ -456,10 +477,10 @@ void launch_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t l
 void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
                      uint32_t* partials, int grid, cudaStream_t s) {
     if (fp32)
-        rht_amax_kernel<float><<<grid, kAmaxThreads, 0, s>>>(static_cast<const float*>(x), rows, cols, ldx, rht_seed,
+        rht_amax_kernel<float><<<grid, kRhtAmaxThreads, 0, s>>>(static_cast<const float*>(x), rows, cols, ldx, rht_seed,
                                                              partials);
     else
-        rht_amax_kernel<__nv_bfloat16><<<grid, kAmaxThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows,
+        rht_amax_kernel<__nv_bfloat16><<<grid, kRhtAmaxThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows,
                                                                      cols, ldx, rht_seed, partials);
 }
 
