@@ -74,11 +74,11 @@ typedef enum { NVFP4_RTN = 0, NVFP4_SR = 1 } nvfp4_round;
  * Block-scale layouts.
  *   NVFP4_SCALES_LINEAR: byte (r, kb) at r * (cols/16) + kb, where kb = c/16.
  *     For 16x16 blocks the scale of tile (r/16, kb) is repeated on each of
- *     the tile's 16 rows, so both layouts index scales per row.  This is the
- *     layout nvfp4_gemm reads (one 16-byte load per row per 256 K elements).
- *   NVFP4_SCALES_MMA: 512-byte atoms of 128 rows x 4 K blocks, the source
- *     layout of a tcgen05.cp.32x128b.warpx4 scale copy, for consumers that
- *     stage scales that way; with n_katoms = 4 * ceil(cols/256),
+ *     the tile's 16 rows, so both layouts index scales per row.
+ *   NVFP4_SCALES_MMA: 512-byte atoms of 128 rows x 4 K blocks (the source
+ *     layout of a tcgen05.cp.32x128b.warpx4 scale copy).  This is the layout
+ *     nvfp4_gemm reads: the scales of 128 rows x 256 K elements are one
+ *     contiguous 2 KB run.  With n_katoms = 4 * ceil(cols/256),
  *       byte (r, kb) = ((r/128) * n_katoms + kb/4) * 512
  *                      + (r%32) * 16 + ((r/32)%4) * 4 + kb%4.
  *     Padding (rows up to a multiple of 128, K blocks up to n_katoms * 4)
@@ -187,7 +187,8 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
  * a block-scaled FP4 GEMM on the tcgen05 tensor cores with FP32
  * accumulation (blog: Blackwell FP4 tensor cores run the linear layers).
  *   A            [M][K] quantized, B [N][K] quantized, both with
- *                NVFP4_SCALES_LINEAR scales, A->cols == B->cols == K,
+ *                NVFP4_SCALES_MMA scales (16-byte aligned buffers of
+ *                nvfp4_scales_bytes() bytes), A->cols == B->cols == K,
  *                K % 64 == 0.
  *   C            device, [M][ldc] of out_dtype (bf16 or fp32), written whole.
  *   workspace    as nvfp4_quantize (may be NULL with 0 bytes: the GEMM
@@ -206,7 +207,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
  *         RHT along tokens with rht_seed, then dY^T -> dytq (SR) and
  *         X^T -> xtq (RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
  * The context holds caller-allocated quantized buffers; every tensor's
- * rows/cols/ld_codes/scale_layout (LINEAR) must be filled in for the shapes
+ * rows/cols/ld_codes/scale_layout (MMA) must be filled in for the shapes
  * above, and the workspace as for nvfp4_quantize.  X, W, dY are bf16,
  * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
  * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).

@@ -112,7 +112,7 @@ def _stream(stream) -> int:
     return int(stream.cuda_stream)
 
 
-def nvfp4_scales_bytes(rows: int, cols: int, scale_layout: str = "linear") -> int:
+def nvfp4_scales_bytes(rows: int, cols: int, scale_layout: str = "mma") -> int:
     return int(lib().nvfp4_scales_bytes(rows, cols, _LAYOUTS[scale_layout]))
 
 
@@ -154,7 +154,7 @@ class QTensor:
                             self.cols, self.ld_codes, _LAYOUTS[self.scale_layout], 0)
 
 
-def empty_qtensor(rows: int, cols: int, device, scale_layout: str = "linear") -> QTensor:
+def empty_qtensor(rows: int, cols: int, device, scale_layout: str = "mma") -> QTensor:
     ld = ((cols // 2 + 15) // 16) * 16
     codes = torch.empty(rows, ld, dtype=torch.uint8, device=device)
     scales = torch.empty(max(nvfp4_scales_bytes(rows, cols, scale_layout), 16), dtype=torch.uint8, device=device)
@@ -178,7 +178,7 @@ def _check_input(x: torch.Tensor):
 
 
 def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", seed: int = 0, *,
-                   rowwise: bool = True, colwise: bool = False, scale_layout: str = "linear",
+                   rowwise: bool = True, colwise: bool = False, scale_layout: str = "mma",
                    out_rowwise: QTensor | None = None, out_colwise: QTensor | None = None, stream=None):
     """Quantize x [rows][cols]; returns (rowwise QTensor or None, colwise QTensor or None)."""
     _check_input(x)
@@ -198,7 +198,7 @@ def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", see
 
 
 def nvfp4_quantize_noalloc(x: torch.Tensor, block: str = "1x16", round: str = "rtn", seed: int = 0, *,
-                           rowwise: bool = True, colwise: bool = False, scale_layout: str = "linear",
+                           rowwise: bool = True, colwise: bool = False, scale_layout: str = "mma",
                            out_rowwise: QTensor | None = None, out_colwise: QTensor | None = None, stream=None):
     """nvfp4_quantize without a workspace: for callers that cannot allocate
     device memory, the library keeps the amax scratch in a fixed device array
@@ -219,7 +219,7 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, block: str = "1x16", round: str = "r
 
 
 def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,
-                       scale_layout: str = "linear", out_colwise: QTensor | None = None, stream=None) -> QTensor:
+                       scale_layout: str = "mma", out_colwise: QTensor | None = None, stream=None) -> QTensor:
     """16-point RHT along the rows of x, then colwise 1x16 quantization of the result's transpose."""
     _check_input(x)
     rows, cols = x.shape

@@ -277,8 +277,10 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     if (A->cols != B->cols)
         return fail(NVFP4_ERR_INVALID_ARG, "K mismatch: %lld vs %lld", (long long)A->cols, (long long)B->cols);
     if (A->cols % 64) return fail(NVFP4_ERR_INVALID_ARG, "K %lld not a multiple of 64", (long long)A->cols);
-    if (A->scale_layout != NVFP4_SCALES_LINEAR || B->scale_layout != NVFP4_SCALES_LINEAR)
-        return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands need NVFP4_SCALES_LINEAR scales");
+    if (A->scale_layout != NVFP4_SCALES_MMA || B->scale_layout != NVFP4_SCALES_MMA)
+        return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands need NVFP4_SCALES_MMA scales");
+    if (!aligned16(A->scales) || !aligned16(B->scales))
+        return fail(NVFP4_ERR_INVALID_ARG, "GEMM scale buffers must be 16-byte aligned");
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
         return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
     const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
@@ -313,8 +315,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
 static nvfp4_status check_linear_tensor(const nvfp4_tensor* t, int64_t rows, int64_t cols, const char* name) {
     nvfp4_status st = check_out(t, rows, cols, name);
     if (st) return st;
-    if (t->scale_layout != NVFP4_SCALES_LINEAR)
-        return fail(NVFP4_ERR_INVALID_ARG, "%s: needs NVFP4_SCALES_LINEAR", name);
+    if (t->scale_layout != NVFP4_SCALES_MMA)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: needs NVFP4_SCALES_MMA", name);
     return NVFP4_OK;
 }
 

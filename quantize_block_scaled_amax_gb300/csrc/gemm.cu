@@ -10,21 +10,24 @@
 //
 // Tile 128 x 256 (M x N), K staged 256 at a time; one persistent CTA per SM,
 // 16 warps in four warpgroups:
-//   warp 0      TMA producer: A and B code tiles (128-byte swizzle) into a
-//               4-stage smem ring (48 KB per stage), plus B's block scales
-//               for the stage (a 16-byte x 256-row box) when K % 256 == 0.
+//   warp 0      producer: A and B code tiles by TMA (128-byte swizzle) into
+//               a 4-stage smem ring, and the stage's block scales (MMA
+//               layout: three contiguous 2 KB runs of 512-byte atoms, A's
+//               128 rows and B's two 128-row groups) by bulk copies, first,
+//               on their own barrier.  54 KB per stage.
 //   warp 1      TMEM owner and MMA issuer: four
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //               (M=128, N=256, K=64) per stage into one TMEM accumulator.
-//   warps 4-7   scale-factor writers, one per TMEM lane quarter: A scales
-//               come straight from the row-major scale buffer (one 16-byte
-//               load per row per stage, prefetched 3 stages ahead), B scales
-//               from the stage's smem box; both go into TMEM with
-//               tcgen05.st (layout at scale_role).  Scale copies through the
-//               tensor pipe (tcgen05.cp) would serialize with the MMAs.
+//   warps 4-7   scale-factor writers, one per TMEM lane quarter: they read
+//               the stage's scale atoms from smem and write them into TMEM
+//               with tcgen05.st (layout at scale_role).  Scale copies through
+//               the tensor pipe (tcgen05.cp) would serialize with the MMAs,
+//               and a TMA box of 256 rows x 16 bytes costs about one cycle
+//               per row of the SM's copy bandwidth, so the scales come as
+//               long contiguous runs.
 //   warps 8-15  epilogue: two warps per lane quarter drain 128 accumulator
 //               columns each with tcgen05.ld, release the accumulator, then
-//               scale by alpha, convert and store through a 2 KB swizzled
+//               scale by alpha, convert and store through a 1 KB swizzled
 //               smem staging tile with TMA tensor stores.
 // Registers: 128 per thread (512 threads fill the register file); the
 // epilogue holds its 128 accumulator words with a few words spilled.
@@ -51,19 +54,14 @@ constexpr int kMmaK = 64;          // K per tcgen05.mma (FP4)
 constexpr int kMmaPerStage = BK / kMmaK;
 constexpr int kATileBytes = BM * BKB;      // 16 KB
 constexpr int kBTileBytes = BN * BKB;      // 32 KB
-constexpr int kSfbTileBytes = BN * 16;     // 4 KB: 256 rows x 16 scales
-constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfbTileBytes;
+constexpr int kSfAtomBytes = 512;           // 128 rows x 4 K blocks (MMA scale layout)
+constexpr int kSfRunBytes = 4 * kSfAtomBytes;  // one 128-row group, one stage (16 K blocks)
+constexpr int kSfStageBytes = 3 * kSfRunBytes; // A, B rows 0-127, B rows 128-255
+constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfStageBytes;
 constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
-constexpr int kStagingBytes = 32 * 64;     // per epilogue warp: 32 rows x 64 bytes
-constexpr int kSfaAhead = 3;               // stages of A scales prefetched in registers
-#ifndef NVFP4_GEMM_CLUSTER
-#define NVFP4_GEMM_CLUSTER 1
-#endif
-constexpr int kCluster = NVFP4_GEMM_CLUSTER;  // CTAs sharing one B tile (multicast)
-constexpr int kBSlice = BN / kCluster;       // B rows each CTA of a cluster loads
-static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster size");
+constexpr int kStagingBytes = 32 * 32;     // per epilogue warp: 32 rows x 32 bytes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns
 constexpr uint32_t kSfaCols = kMmaPerStage * 4;         // 4 columns per MMA
@@ -74,7 +72,7 @@ static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 struct __align__(8) SharedState {
     uint64_t full[kStages];     // A/B tiles landed (TMA transaction count)
-    uint64_t sfb_full[kStages]; // B scales of the stage landed (TMA transaction count)
+    uint64_t sf_in[kStages];    // scale atoms of the stage landed (bulk-copy transaction count)
     uint64_t sf_full[kStages];  // scales written to TMEM (4 scale warps)
     uint64_t empty[kStages];    // MMAs of the stage done (tcgen05.commit)
     uint64_t acc_full;          // accumulator complete (tcgen05.commit)
@@ -228,111 +226,68 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 16 block scales (one stage: 256 K elements) of one row from the row-major
-// scale buffer; blocks at or past nkb read as 0.  vec: 16-byte aligned rows.
-__device__ __forceinline__ uint4 load_row_scales(const uint8_t* row, int kt, int nkb, bool vec) {
-    const int b0 = 16 * kt;
-    if (vec && b0 + 16 <= nkb) return __ldg(reinterpret_cast<const uint4*>(row + b0));
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + b0);
-    uint4 r = make_uint4(0u, 0u, 0u, 0u);
-    if (b0 + 4 <= nkb) r.x = __ldg(w);
-    if (b0 + 8 <= nkb) r.y = __ldg(w + 1);
-    if (b0 + 12 <= nkb) r.z = __ldg(w + 2);
-    if (b0 + 16 <= nkb) r.w = __ldg(w + 3);
-    return r;
-}
-
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
+// Contiguous global -> shared copy (16-byte aligned, size a multiple of 16)
+// completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ int cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return (int)r;
 }
 
 // ---- the kernel ----------------------------------------------------------------
 struct Params {
-    const uint8_t* a_scales;  // [M][K/16] row-major E4M3
-    const uint8_t* b_scales;  // [N][K/16]
+    const uint8_t* a_scales;  // MMA layout (512-byte atoms), rows padded to 128
+    const uint8_t* b_scales;
     const float* a_amax;
     const float* b_amax;
     int M, N, K;
     int num_m, num_n, num_k;  // tiles
-    int nkb;                  // K / 16
-    int sf_vec;               // rows of the scale buffers are 16-byte aligned (B scales come by TMA)
+    int n_katoms;             // atoms per 128-row group: 4 * ceil(K / 256)
+    int b_groups;             // 128-row groups of B: ceil(N / 128)
     int out_fp32;
     uint32_t* status;
 };
 
-// Tile schedule: a cluster of kCluster CTAs takes kCluster consecutive M
-// tiles of one N tile (its "group"); clusters walk the groups with M fastest.
-// Every CTA of a cluster visits the same groups in the same order.  A CTA
-// whose M tile lies past the matrix still runs (its A rows read as zero and
-// its stores fall outside C), because its share of the B tile feeds the
-// other CTAs.
+// Tile schedule: CTA c takes tiles c, c + gridDim.x, ... with M fastest.
 struct Sched {
-    int rank, cid, nclusters, num_mg, num_groups;
-    __device__ explicit Sched(const Params& p) {
-        rank = kCluster > 1 ? cluster_rank() : 0;
-        cid = (int)blockIdx.x / kCluster;
-        nclusters = (int)gridDim.x / kCluster;
-        num_mg = (p.num_m + kCluster - 1) / kCluster;
-        num_groups = num_mg * p.num_n;
+    int num_tiles;
+    __device__ explicit Sched(const Params& p) { num_tiles = p.num_m * p.num_n; }
+    __device__ int count() const {
+        return (int)blockIdx.x < num_tiles ? (num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     }
-    __device__ int count() const { return cid < num_groups ? (num_groups - cid + nclusters - 1) / nclusters : 0; }
-    __device__ void tile(int i, int& mb, int& nb) const {
-        const int g = cid + i * nclusters;
-        nb = g / num_mg;
-        mb = (g % num_mg) * kCluster + rank;
+    __device__ void tile(int i, const Params& p, int& mb, int& nb) const {
+        const int t = (int)blockIdx.x + i * (int)gridDim.x;
+        nb = t / p.num_m;
+        mb = t - nb * p.num_m;
     }
 };
 
-__device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
-                                              const CUtensorMap* tmap_sfb, const Params& p, SharedState* ss, uint8_t* sA,
-                                              uint8_t* sB, uint8_t* sSfb) {
+__device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
+                                              SharedState* ss, uint8_t* sA, uint8_t* sB, uint8_t* sSf) {
     const Sched S(p);
-    const uint16_t mask = (uint16_t)((1u << kCluster) - 1u);
     uint32_t it = 0;
     for (int i = 0; i < S.count(); ++i) {
         int mb, nb;
-        S.tile(i, mb, nb);
+        S.tile(i, p, mb, nb);
+        const bool b_hi = 2 * nb + 1 < p.b_groups;  // B rows 128..255 of the tile exist
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1u;
-            // free in every CTA of the cluster: the multicasts below write all of them
             if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
-            const int rb = nb * BN + S.rank * kBSlice;
-            if (p.sf_vec) {
-                // the small scale box first: the scale writers need only it
-                mbar_arrive_expect_tx(&ss->sfb_full[s], kSfbTileBytes);
-                uint8_t* dst = sSfb + s * kSfbTileBytes + S.rank * kBSlice * 16;
-                if (kCluster > 1) tma_load_2d_mc(dst, tmap_sfb, &ss->sfb_full[s], kt * 16, rb, mask);
-                else tma_load_2d(dst, tmap_sfb, &ss->sfb_full[s], kt * 16, rb);
-            }
+            // the scale runs first: the scale writers need only them
+            uint8_t* sf = sSf + s * kSfStageBytes;
+            mbar_arrive_expect_tx(&ss->sf_in[s], (b_hi ? 3 : 2) * kSfRunBytes);
+            bulk_load(sf, p.a_scales + ((size_t)mb * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes, &ss->sf_in[s]);
+            bulk_load(sf + kSfRunBytes, p.b_scales + ((size_t)(2 * nb) * p.n_katoms + 4 * kt) * kSfAtomBytes,
+                      kSfRunBytes, &ss->sf_in[s]);
+            if (b_hi)
+                bulk_load(sf + 2 * kSfRunBytes,
+                          p.b_scales + ((size_t)(2 * nb + 1) * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes,
+                          &ss->sf_in[s]);
             mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
             tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kt * BKB, mb * BM);
-            uint8_t* bdst = sB + s * kBTileBytes + S.rank * kBSlice * BKB;
-            if (kCluster > 1) tma_load_2d_mc(bdst, tmap_b, &ss->full[s], kt * BKB, rb, mask);
-            else tma_load_2d(bdst, tmap_b, &ss->full[s], kt * BKB, rb);
+            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kt * BKB, nb * BN);
         }
     }
 }
@@ -340,7 +295,6 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
 __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
                                          uint32_t tmem_base) {
     const Sched S(p);
-    const uint16_t mask = (uint16_t)((1u << kCluster) - 1u);
     const uint32_t idesc = instr_desc_nvf4(BM, BN);
     const uint32_t sf_base = tmem_base + kAccCols;
     uint32_t it = 0, tc = 0;
@@ -362,9 +316,7 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
                 const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
                 mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
             }
-            // the stage is free once every CTA of the cluster is done with it
-            if (kCluster > 1) mma_commit_mc(&ss->empty[s], mask);
-            else mma_commit(&ss->empty[s]);
+            mma_commit(&ss->empty[s]);
         }
         mma_commit(&ss->acc_full);
     }
@@ -378,92 +330,75 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
 // Writer warp q (lanes 32q .. 32q+31 of TMEM), lane l: A row 32q + l, and B
 // rows 32c + l for c = 0..7.  Per stage, MMA j reads A words at columns
 // 4j..4j+3 (the lane's word is written into all four) and B words at
-// 8j..8j+7.
-__device__ __forceinline__ uint4 stage_a_scales(const Params& p, int it, int q, int lane) {
-    const Sched S(p);
-    const int i = it / p.num_k, kt = it % p.num_k;
-    if (i >= S.count()) return make_uint4(0u, 0u, 0u, 0u);
-    int mb, nb;
-    S.tile(i, mb, nb);
-    const int ra = mb * BM + 32 * q + lane;
-    if (ra >= p.M) return make_uint4(0u, 0u, 0u, 0u);
-    return load_row_scales(p.a_scales + (size_t)ra * p.nkb, kt, p.nkb, p.sf_vec);
-}
-
-__device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, const uint8_t* sSfb, uint32_t tmem_base,
+// 8j..8j+7.  In smem, atom j of a 128-row group holds row 32c + l's four
+// scales of MMA j at byte 16 l + 4 c, so lane l reads A's word with one
+// 4-byte load per MMA and four B words (c = 0..3 of a group) with one
+// 16-byte load per group and MMA.
+__device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, const uint8_t* sSf, uint32_t tmem_base,
                                            int q, int lane) {
     const Sched S(p);
-    const int total = S.count() * p.num_k;
     const uint32_t sf_base = tmem_base + kAccCols;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    // A scales run kSfaAhead stages ahead in registers to hide the L2 latency
-    uint4 a0 = stage_a_scales(p, 0, q, lane), a1 = stage_a_scales(p, 1, q, lane), a2 = stage_a_scales(p, 2, q, lane);
-    for (int it = 0; it < total; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        const uint4 wa = a0;
-        a0 = a1;
-        a1 = a2;
-        a2 = stage_a_scales(p, it + kSfaAhead, q, lane);
-        uint4 wb[8];
-        if (p.sf_vec) {
-            // the B scales of this stage arrive with the code tiles
-            if (!warp_wait(&ss->sfb_full[s], ph, ss, p.status)) return;
-            const uint8_t* rows = sSfb + s * kSfbTileBytes + lane * 16;
+    uint32_t it = 0;
+    for (int i = 0; i < S.count(); ++i) {
+        int mb, nb;
+        S.tile(i, p, mb, nb);
+        const bool b_hi = 2 * nb + 1 < p.b_groups;
+        for (int kt = 0; kt < p.num_k; ++kt, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1u;
+            if (!warp_wait(&ss->sf_in[s], ph, ss, p.status)) return;
+            const uint8_t* sf = sSf + s * kSfStageBytes + lane * 16;
+            uint32_t wa[kMmaPerStage];
+            uint4 wb[2][kMmaPerStage];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) wb[c] = *reinterpret_cast<const uint4*>(rows + 32 * 16 * c);
-        } else {
-            int mb, nb;
-            S.tile(it / p.num_k, mb, nb);
-            const int kt = it % p.num_k;
-            const int rb = nb * BN + lane;
-            const uint8_t* pb = p.b_scales + (size_t)rb * p.nkb;
+            for (int j = 0; j < kMmaPerStage; ++j) {
+                wa[j] = *reinterpret_cast<const uint32_t*>(sf + j * kSfAtomBytes + 4 * q);
+                wb[0][j] = *reinterpret_cast<const uint4*>(sf + kSfRunBytes + j * kSfAtomBytes);
+                wb[1][j] = b_hi ? *reinterpret_cast<const uint4*>(sf + 2 * kSfRunBytes + j * kSfAtomBytes)
+                                : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // the TMEM slot is free once the MMAs that read it four stages ago are done
+            if (!warp_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+            tc_fence_after();
+            const uint32_t col = lane_addr + sf_base + s * kSfColsPerStage;
+            const uint32_t va[16] = {wa[0], wa[0], wa[0], wa[0], wa[1], wa[1], wa[1], wa[1],
+                                     wa[2], wa[2], wa[2], wa[2], wa[3], wa[3], wa[3], wa[3]};
+            tmem_st_x16(col, va);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                wb[c] = rb + 32 * c < p.N ? load_row_scales(pb + (size_t)32 * c * p.nkb, kt, p.nkb, false)
-                                          : make_uint4(0u, 0u, 0u, 0u);
+            for (int h = 0; h < 2; ++h) {  // MMAs 2h and 2h + 1
+                uint32_t vb[16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint4 lo = wb[0][2 * h + u], hi = wb[1][2 * h + u];
+                    vb[8 * u + 0] = lo.x; vb[8 * u + 1] = lo.y; vb[8 * u + 2] = lo.z; vb[8 * u + 3] = lo.w;
+                    vb[8 * u + 4] = hi.x; vb[8 * u + 5] = hi.y; vb[8 * u + 6] = hi.z; vb[8 * u + 7] = hi.w;
+                }
+                tmem_st_x16(col + kSfaCols + 16 * h, vb);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss->sf_full[s]);
         }
-        if (!warp_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
-        tc_fence_after();
-        const uint32_t col = lane_addr + sf_base + s * kSfColsPerStage;
-        const uint32_t va[16] = {wa.x, wa.x, wa.x, wa.x, wa.y, wa.y, wa.y, wa.y,
-                                 wa.z, wa.z, wa.z, wa.z, wa.w, wa.w, wa.w, wa.w};
-        tmem_st_x16(col, va);
-        uint32_t vb[16];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            vb[c] = wb[c].x;
-            vb[8 + c] = wb[c].y;
-        }
-        tmem_st_x16(col + kSfaCols, vb);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            vb[c] = wb[c].z;
-            vb[8 + c] = wb[c].w;
-        }
-        tmem_st_x16(col + kSfaCols + 16, vb);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ss->sf_full[s]);
     }
 }
 
 // Epilogue warp e: lane quarter q = warp % 4, accumulator half h (columns
-// [128h, 128h + 128)).  Rows leave through a 32 x 64-byte staging tile in
-// the 64-byte swizzle (16-byte chunk j of row r at position j ^ ((r/2) % 4)),
-// one TMA store per 64 bytes of every row.
+// [128h, 128h + 128)).  Rows leave through a 32 x 32-byte staging tile in
+// the 32-byte swizzle (16-byte chunk j of row r at position j ^ ((r/4) % 2)),
+// one TMA store per 32 bytes of every row.
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
                                               uint8_t* stage, uint32_t tmem_base, int q, int h, int lane) {
     const Sched S(p);
     const float alpha = __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
-    uint8_t* row_base = stage + lane * 64;
-    const int sw = (lane >> 1) & 3;
+    uint8_t* row_base = stage + lane * 32;
+    const int sw = (lane >> 2) & 1;
     uint32_t tc = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
         int mb, nb;
-        S.tile(i, mb, nb);
+        S.tile(i, p, mb, nb);
         if (!warp_wait(&ss->acc_full, tc & 1u, ss, p.status)) break;
         tc_fence_after();
         uint32_t acc[128];
@@ -476,14 +411,15 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
 
         const int y = mb * BM + 32 * q;
         const int col0 = nb * BN + 128 * h;
+        const bool rows_in = y < p.M;
         if (p.out_fp32) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16 floats per 64-byte row
+            for (int c = 0; c < 16; ++c) {  // 8 floats per 32-byte row
                 if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t* a = acc + 16 * c + 4 * j;
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t* a = acc + 8 * c + 4 * j;
                     const uint4 v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
                                                __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
                                                __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
@@ -492,19 +428,19 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0 && y < p.M && col0 + 16 * c < p.N) {
-                    tma_store_2d(tmap_c, stage, col0 + 16 * c, y);
+                if (lane == 0 && rows_in && col0 + 8 * c < p.N) {
+                    tma_store_2d(tmap_c, stage, col0 + 8 * c, y);
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // 32 bf16 per 64-byte row
+            for (int c = 0; c < 8; ++c) {  // 16 bf16 per 32-byte row
                 if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t* a = acc + 32 * c + 8 * j;
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t* a = acc + 16 * c + 8 * j;
                     const uint4 v = make_uint4(
                         pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
                         pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
@@ -514,8 +450,8 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0 && y < p.M && col0 + 32 * c < p.N) {
-                    tma_store_2d(tmap_c, stage, col0 + 32 * c, y);
+                if (lane == 0 && rows_in && col0 + 16 * c < p.N) {
+                    tma_store_2d(tmap_c, stage, col0 + 16 * c, y);
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
@@ -527,14 +463,13 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
 
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sfb,
-                     const Params p) {
+                     const __grid_constant__ CUtensorMap tmap_c, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + kStages * kATileBytes;
-    uint8_t* sSfb = sB + kStages * kBTileBytes;
-    uint8_t* sStage = sSfb + kStages * kSfbTileBytes;
+    uint8_t* sSf = sB + kStages * kBTileBytes;
+    uint8_t* sStage = sSf + kStages * kSfStageBytes;
     SharedState* ss = reinterpret_cast<SharedState*>(sStage + kEpiWarps * kStagingBytes);
 
     const int warp = threadIdx.x >> 5;
@@ -543,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ss->full[s], 1);
-            mbar_init(&ss->sfb_full[s], 1);
+            mbar_init(&ss->sf_in[s], 1);
             mbar_init(&ss->sf_full[s], kSfWarps);
-            mbar_init(&ss->empty[s], kCluster);
+            mbar_init(&ss->empty[s], 1);
         }
         mbar_init(&ss->acc_full, 1);
         mbar_init(&ss->acc_empty, kEpiWarps);
@@ -554,7 +489,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_c) : "memory");
-        if (p.sf_vec) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_sfb) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -564,28 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (kCluster > 1) cluster_sync();  // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = ss->tmem_base;
 
     if (warp < 8) {
         if (warp == 0) {
-            if (lane == 0) producer_role(&tmap_a, &tmap_b, &tmap_sfb, p, ss, sA, sB, sSfb);
+            if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, sA, sB, sSf);
         } else if (warp == 1) {
             if (lane == 0) mma_role(p, ss, sA, sB, tmem_base);
         } else if (warp >= 4) {
-            scale_role(p, ss, sSfb, tmem_base, warp & 3, lane);
+            scale_role(p, ss, sSf, tmem_base, warp & 3, lane);
         }
     } else {
         const int e = warp - 8;
         epilogue_role(&tmap_c, p, ss, sStage + e * kStagingBytes, tmem_base, warp & 3, e >> 2, lane);
     }
 
-    // Drain: every role reaches this barrier (every CTA of the cluster: no
-    // peer may still multicast into this CTA), then warp 1 frees TMEM.
+    // Drain: every role reaches this barrier, then warp 1 frees TMEM.
     tc_fence_before();
     __syncthreads();
-    if (kCluster > 1) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
@@ -632,7 +563,6 @@ int make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int64_t
 }
 
 bool g_attr_set[64] = {};
-int g_max_clusters[64] = {};
 std::mutex g_attr_mu;
 
 }  // namespace gemm
@@ -644,32 +574,21 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
         *msg = "dimension exceeds 2^31";
         return -1;
     }
-    CUtensorMap ta, tb, tcm, tsf;
+    CUtensorMap ta, tb, tcm;
     if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.M, g.K / 2, g.lda, BKB, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg))
         return 1;
-    if (make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, kBSlice,
+    if (make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, BN,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg))
         return 1;
     if (g.out_fp32) {
-        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.c, g.M, g.N, g.ldc * 4, 16, 32,
-                     CU_TENSOR_MAP_SWIZZLE_64B, msg))
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.c, g.M, g.N, g.ldc * 4, 8, 32,
+                     CU_TENSOR_MAP_SWIZZLE_32B, msg))
             return 1;
     } else {
-        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
-                     CU_TENSOR_MAP_SWIZZLE_64B, msg))
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 16, 32,
+                     CU_TENSOR_MAP_SWIZZLE_32B, msg))
             return 1;
-    }
-    const int nkb = (int)(g.K / 16);
-    const bool sf_vec = (nkb % 16 == 0) &&
-                        ((reinterpret_cast<uintptr_t>(g.a_scales) | reinterpret_cast<uintptr_t>(g.b_scales)) % 16 == 0);
-    if (sf_vec) {
-        // B scales, [N][K/16] bytes: a 16-byte x kBSlice-row box per CTA per stage
-        if (make_map(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_scales, g.N, nkb, nkb, 16, kBSlice,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, msg))
-            return 1;
-    } else {
-        tsf = ta;  // unused
     }
     {
         int dev = 0;
@@ -693,44 +612,14 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.num_m = (int)((g.M + BM - 1) / BM);
     p.num_n = (int)((g.N + BN - 1) / BN);
     p.num_k = (int)((g.K + BK - 1) / BK);
-    p.nkb = nkb;
-    p.sf_vec = sf_vec ? 1 : 0;
+    p.n_katoms = 4 * p.num_k;
+    p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
     p.status = g.status;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // persistent: as many clusters as fit at once, at most one per tile group
-    int max_clusters = 0;
-    {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lk(g_attr_mu);
-        if (dev >= 0 && dev < 64 && g_max_clusters[dev] == 0) {
-            cfg.gridDim = dim3((unsigned)(g.num_sms / kCluster * kCluster));
-            int n = 0;
-            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_kernel, &cfg);
-            if (e != cudaSuccess || n <= 0) {
-                (void)cudaGetLastError();
-                n = g.num_sms / kCluster;
-            }
-            g_max_clusters[dev] = n;
-        }
-        max_clusters = (dev >= 0 && dev < 64) ? g_max_clusters[dev] : g.num_sms / kCluster;
-    }
-    const int groups = ((p.num_m + kCluster - 1) / kCluster) * p.num_n;
-    const int clusters = groups < max_clusters ? groups : max_clusters;
-    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
-    cudaError_t e = cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel, ta, tb, tcm, tsf, p);
-    if (e != cudaSuccess) return (int)e;
+    // persistent: one CTA per SM, at most one per tile
+    const int64_t tiles = (int64_t)p.num_m * p.num_n;
+    const int grid = (int)(tiles < g.num_sms ? tiles : g.num_sms);
+    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tcm, p);
     return (int)cudaGetLastError();
 }
 

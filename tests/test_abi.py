@@ -92,11 +92,13 @@ def test_host_argument_checks_need_no_gpu(L):
 
 def test_gemm_argument_checks_need_no_gpu(L):
     import quantize_block_scaled_amax_gb300 as q
-    a = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 0, 0)
-    b = q.nvfp4_tensor(16, 16, 16, 64, 64, 32, 0, 0)      # K mismatch
+    a = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 1, 0)
+    b = q.nvfp4_tensor(16, 16, 16, 64, 64, 32, 1, 0)      # K mismatch
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
-    b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 1, 0)     # MMA-atom scales
+    b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 0, 0)     # row-major (LINEAR) scales
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
-    a = q.nvfp4_tensor(16, 16, 16, 128, 96, 48, 0, 0)     # K % 64 != 0
-    b = q.nvfp4_tensor(16, 16, 16, 64, 96, 48, 0, 0)
+    b = q.nvfp4_tensor(16, 24, 16, 64, 128, 64, 1, 0)     # scale buffer not 16-byte aligned
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
+    a = q.nvfp4_tensor(16, 16, 16, 128, 96, 48, 1, 0)     # K % 64 != 0
+    b = q.nvfp4_tensor(16, 16, 16, 64, 96, 48, 1, 0)
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
