@@ -11,10 +11,12 @@
 // Tile 128 x 256 (M x N), K staged 256 at a time; one persistent CTA per SM,
 // 16 warps in four warpgroups:
 //   warp 0      producer: A and B code tiles by TMA (128-byte swizzle) into
-//               a 4-stage smem ring, and the stage's block scales (MMA
-//               layout: three contiguous 2 KB runs of 512-byte atoms, A's
-//               128 rows and B's two 128-row groups) by bulk copies, first,
-//               on their own barrier.  54 KB per stage.
+//               a 4-stage smem ring (48 KB per stage).
+//   warp 2      scale producer: the stage's block scales (MMA layout: three
+//               contiguous 2 KB runs of 512-byte atoms, A's 128 rows and B's
+//               two 128-row groups) by bulk copies into a 4-slot ring of its
+//               own, whose slots free as soon as the scale writers have read
+//               them, so the scales run ahead of the code tiles.
 //   warp 1      TMEM owner and MMA issuer: four
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //               (M=128, N=256, K=64) per stage into one TMEM accumulator.
@@ -73,6 +75,7 @@ static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 struct __align__(8) SharedState {
     uint64_t full[kStages];     // A/B tiles landed (TMA transaction count)
     uint64_t sf_in[kStages];    // scale atoms of the stage landed (bulk-copy transaction count)
+    uint64_t sf_free[kStages];  // scale atoms of the stage read out of smem (4 scale warps)
     uint64_t sf_full[kStages];  // scales written to TMEM (4 scale warps)
     uint64_t empty[kStages];    // MMAs of the stage done (tcgen05.commit)
     uint64_t acc_full;          // accumulator complete (tcgen05.commit)
@@ -264,7 +267,24 @@ struct Sched {
 };
 
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
-                                              SharedState* ss, uint8_t* sA, uint8_t* sB, uint8_t* sSf) {
+                                              SharedState* ss, uint8_t* sA, uint8_t* sB) {
+    const Sched S(p);
+    uint32_t it = 0;
+    for (int i = 0; i < S.count(); ++i) {
+        int mb, nb;
+        S.tile(i, p, mb, nb);
+        for (int kt = 0; kt < p.num_k; ++kt, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1u;
+            if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+            mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
+            tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kt * BKB, mb * BM);
+            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kt * BKB, nb * BN);
+        }
+    }
+}
+
+__device__ __forceinline__ void scale_producer_role(const Params& p, SharedState* ss, uint8_t* sSf) {
     const Sched S(p);
     uint32_t it = 0;
     for (int i = 0; i < S.count(); ++i) {
@@ -274,8 +294,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1u;
-            if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
-            // the scale runs first: the scale writers need only them
+            if (!mbar_wait(&ss->sf_free[s], ph ^ 1u, ss, p.status)) return;
             uint8_t* sf = sSf + s * kSfStageBytes;
             mbar_arrive_expect_tx(&ss->sf_in[s], (b_hi ? 3 : 2) * kSfRunBytes);
             bulk_load(sf, p.a_scales + ((size_t)mb * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes, &ss->sf_in[s]);
@@ -285,9 +304,6 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
                 bulk_load(sf + 2 * kSfRunBytes,
                           p.b_scales + ((size_t)(2 * nb + 1) * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes,
                           &ss->sf_in[s]);
-            mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
-            tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kt * BKB, mb * BM);
-            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kt * BKB, nb * BN);
         }
     }
 }
@@ -358,6 +374,8 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
                 wb[1][j] = b_hi ? *reinterpret_cast<const uint4*>(sf + 2 * kSfRunBytes + j * kSfAtomBytes)
                                 : make_uint4(0u, 0u, 0u, 0u);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss->sf_free[s]);
             // the TMEM slot is free once the MMAs that read it four stages ago are done
             if (!warp_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
             tc_fence_after();
@@ -479,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ss->full[s], 1);
             mbar_init(&ss->sf_in[s], 1);
+            mbar_init(&ss->sf_free[s], kSfWarps);
             mbar_init(&ss->sf_full[s], kSfWarps);
             mbar_init(&ss->empty[s], 1);
         }
@@ -503,7 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         if (warp == 0) {
-            if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, sA, sB, sSf);
+            if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, sA, sB);
+        } else if (warp == 2) {
+            if (lane == 0) scale_producer_role(p, ss, sSf);
         } else if (warp == 1) {
             if (lane == 0) mma_role(p, ss, sA, sB, tmem_base);
         } else if (warp >= 4) {
