@@ -110,6 +110,14 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_oracle_e2m1_encode_sr_array.argtypes = [f32p, u32p, i64, u8p]
             L.nvfp4_oracle_e4m3_encode_array.restype = None
             L.nvfp4_oracle_e4m3_encode_array.argtypes = [f32p, i64, u8p]
+            L.nvfp4_oracle_e8m0_decode.restype = ctypes.c_double
+            L.nvfp4_oracle_e8m0_decode.argtypes = [ctypes.c_uint32]
+            L.nvfp4_oracle_mx_block_scale.restype = ctypes.c_uint32
+            L.nvfp4_oracle_mx_block_scale.argtypes = [ctypes.c_float]
+            L.nvfp4_oracle_mx_quantize.restype = ctypes.c_int
+            L.nvfp4_oracle_mx_quantize.argtypes = [f32p, i64, i64, i64, ctypes.c_int, ctypes.c_uint64, u8p, u8p]
+            L.nvfp4_oracle_mx_dequantize.restype = ctypes.c_int
+            L.nvfp4_oracle_mx_dequantize.argtypes = [u8p, u8p, i64, i64, f64p]
             _lib = L
     return _lib
 
@@ -242,6 +250,14 @@ def logical_tensor(x: np.ndarray, layout: str = "row", rht_seed: int | None = No
     return t
 
 
+def e8m0_decode(b: int) -> float:
+    return lib().nvfp4_oracle_e8m0_decode(int(b))
+
+
+def mx_block_scale(bamax: float) -> int:
+    return lib().nvfp4_oracle_mx_block_scale(float(bamax))
+
+
 def quantize(x: np.ndarray, *, layout: str = "row", block: str = "1x16", rounding: str = "rtn",
              seed: int = 0, rht_seed: int | None = None, rows: tuple[int, int] | None = None,
              logical: np.ndarray | None = None) -> dict:
@@ -249,7 +265,9 @@ def quantize(x: np.ndarray, *, layout: str = "row", block: str = "1x16", roundin
 
     layout  'row': codes describe x, blocks along C, codes [R][C/2].
             'col': codes describe x^T, blocks along R, codes [C][R/2].
-    block   '1x16' or '16x16' (one scale per 16x16 tile of the logical tensor).
+    block   '1x16' or '16x16' (one scale per 16x16 tile of the logical tensor),
+            or 'mx1x32' (MXFP4: 32-element blocks, UE8M0 power-of-two
+            scales, no tensor scale; then amax, s_dec, s_enc are 0, 1, 1).
     rounding 'rtn' (nearest, ties to even) or 'sr' (stochastic, Philox).
     rht_seed apply the 16-point RHT along the logical rows first.
     rows    (start, stop): quantize only those logical rows; the tensor amax
@@ -260,6 +278,8 @@ def quantize(x: np.ndarray, *, layout: str = "row", block: str = "1x16", roundin
     [rows][C/16] for 1x16 and [rows/16][C/16] for 16x16.
     """
     t = logical if logical is not None else logical_tensor(x, layout, rht_seed)
+    if block == "mx1x32":
+        return _mx_quantize(t, rounding, seed, rows)
     block_h = {"1x16": 1, "16x16": 16}[block]
     stochastic = {"rtn": 0, "sr": 1}[rounding]
     nrows_all, cols = t.shape
@@ -279,8 +299,34 @@ def quantize(x: np.ndarray, *, layout: str = "row", block: str = "1x16", roundin
                 s_enc=float(amax3[2]), block_h=block_h, row0=r0)
 
 
+def _mx_quantize(t: np.ndarray, rounding: str, seed: int, rows) -> dict:
+    stochastic = {"rtn": 0, "sr": 1}[rounding]
+    nrows_all, cols = t.shape
+    r0, r1 = (0, nrows_all) if rows is None else rows
+    sub = np.ascontiguousarray(t[r0:r1], dtype=np.float32)
+    n = r1 - r0
+    codes = np.zeros((n, cols // 2), dtype=np.uint8)
+    scales = np.zeros((n, cols // 32), dtype=np.uint8)
+    st = lib().nvfp4_oracle_mx_quantize(_ptr(sub, ctypes.c_float), n, cols, r0, stochastic, int(seed),
+                                        _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    if st:
+        raise OracleError(f"mx quantize: status {st}")
+    return dict(codes=codes, scales=scales, amax=0.0, s_dec=1.0, s_enc=1.0, block_h=1, row0=r0, fmt="mx")
+
+
 def dequantize(q: dict) -> np.ndarray:
-    """x^ = e2m1(code) * e4m3(block scale) * S_dec in float64 (exact)."""
+    """x^ = e2m1(code) * e4m3(block scale) * S_dec in float64 (exact); for
+    MXFP4, x^ = e2m1(code) * 2^(scale - 127)."""
+    if q.get("fmt") == "mx":
+        codes = np.ascontiguousarray(q["codes"], dtype=np.uint8)
+        scales = np.ascontiguousarray(q["scales"], dtype=np.uint8)
+        rows, cols = codes.shape[0], codes.shape[1] * 2
+        out = np.zeros((rows, cols), dtype=np.float64)
+        st = lib().nvfp4_oracle_mx_dequantize(_ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8), rows,
+                                              cols, _ptr(out, ctypes.c_double))
+        if st:
+            raise OracleError(f"mx dequantize: status {st}")
+        return out
     codes = np.ascontiguousarray(q["codes"], dtype=np.uint8)
     scales = np.ascontiguousarray(q["scales"], dtype=np.uint8)
     rows, cols = codes.shape[0], codes.shape[1] * 2

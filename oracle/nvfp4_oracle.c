@@ -342,3 +342,88 @@ int nvfp4_oracle_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t
         }
     return ORACLE_OK;
 }
+
+/* ---- MXFP4: the format NVFP4 is compared against -------------------------
+ * Paper summary page, format paragraph and the explainer's comparison
+ * paragraph: MXFP4 (OCP) groups 32 E2M1 elements under one power-of-two
+ * scale stored as UE8M0, and has no tensor-level scale; its power-of-two
+ * scale can leave the block maximum as low as just above 3, so at worst the
+ * +-4 and +-6 levels go unused.  Reading: the block scale is the smallest
+ * power of two 2^e with 6 * 2^e >= bamax (no element clips), e clamped to
+ * the UE8M0 range [-127, 127]; the code is e + 127.  An all-zero block gets
+ * code 0 and zero elements. */
+
+/* UE8M0 decode: 2^(b - 127); 255 is NaN. */
+double nvfp4_oracle_e8m0_decode(uint32_t b) {
+    if (b == 255u) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* The block scale exponent by search: start below the answer and step up
+ * until 6 * 2^e covers bamax (every comparison exact in FP64). */
+uint32_t nvfp4_oracle_mx_block_scale(float bamax) {
+    double a = (double)bamax;
+    if (!(a > 0.0)) return 0;
+    int ex;
+    (void)frexp(a, &ex); /* a = m * 2^ex, m in [0.5, 1) */
+    int e = ex - 4;      /* 6 * 2^(ex-4) = 0.375 * 2^ex < a */
+    while (6.0 * ldexp(1.0, e) < a) e++;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return (uint32_t)(e + 127);
+}
+
+/* Quantize a [rows][cols] tensor to MXFP4 with 1x32 blocks along cols
+ * (cols % 32 == 0).  Element: v = fl32(x * 2^-e) (a power-of-two scaling),
+ * then the same E2M1 rounding as NVFP4 (nearest-even, or stochastic with the
+ * element's Philox word: element (row0 + r) * cols + c).  Outputs codes
+ * [rows][cols/2] and scales [rows][cols/32] (UE8M0 codes). */
+int nvfp4_oracle_mx_quantize(const float* x, int64_t rows, int64_t cols, int64_t row0, int stochastic,
+                             uint64_t seed, uint8_t* codes, uint8_t* scales) {
+    if (rows < 0 || cols < 0 || cols % 32) return ORACLE_ERR_INVALID;
+    for (int64_t i = 0; i < rows * cols; i++)
+        if (!isfinite(x[i])) return ORACLE_ERR_NONFINITE;
+    int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            float bamax = 0.0f;
+            for (int64_t c = b * 32; c < b * 32 + 32; c++) {
+                float v = fabsf(x[r * cols + c]);
+                if (v > bamax) bamax = v;
+            }
+            uint32_t sb = nvfp4_oracle_mx_block_scale(bamax);
+            scales[r * nb + b] = (uint8_t)sb;
+            double mul = ldexp(1.0, 127 - (int)sb); /* 2^-e */
+            for (int64_t c = b * 32; c < b * 32 + 32; c++) {
+                uint32_t code = 0;
+                if (bamax > 0.0f) {
+                    float v = f32((double)x[r * cols + c] * mul);
+                    if (stochastic) {
+                        uint64_t i = (uint64_t)(row0 + r) * (uint64_t)cols + (uint64_t)c;
+                        code = nvfp4_oracle_e2m1_encode_sr(v, nvfp4_oracle_sr_bits(seed, i));
+                    } else {
+                        code = nvfp4_oracle_e2m1_encode_rtn(v);
+                    }
+                }
+                uint8_t* byte = &codes[r * (cols / 2) + c / 2];
+                if (c % 2 == 0) *byte = (uint8_t)((*byte & 0xF0u) | code);
+                else            *byte = (uint8_t)((*byte & 0x0Fu) | (code << 4));
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* MXFP4 dequantize: x^ = e2m1(code) * 2^(sb - 127), exact in FP64. */
+int nvfp4_oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                               double* out) {
+    if (rows < 0 || cols % 32) return ORACLE_ERR_INVALID;
+    int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) {
+            uint32_t byte = codes[r * (cols / 2) + c / 2];
+            uint32_t code = (c % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+            out[r * cols + c] = nvfp4_oracle_e2m1_decode(code) * nvfp4_oracle_e8m0_decode(scales[r * nb + c / 32]);
+        }
+    return ORACLE_OK;
+}
