@@ -67,7 +67,22 @@ typedef enum {
 
 typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
 typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
-typedef enum { NVFP4_BLOCK_1x16 = 0, NVFP4_BLOCK_16x16 = 1 } nvfp4_block;
+typedef enum { NVFP4_BLOCK_1x16 = 0, NVFP4_BLOCK_16x16 = 1, NVFP4_BLOCK_MX1x32 = 2 } nvfp4_block;
+
+/*
+ * Element formats of a quantized tensor (nvfp4_tensor.format).
+ *   NVFP4_FORMAT_NVFP4: E2M1 codes, one E4M3 scale per 16 elements, one FP32
+ *     tensor scale (paper page, format paragraph).
+ *   NVFP4_FORMAT_MXFP4: the format NVFP4 is compared against (paper page,
+ *     format paragraph; explainer page, comparison paragraph): E2M1 codes,
+ *     one power-of-two UE8M0 scale per 32 elements (2^(code - 127), the
+ *     smallest power of two 2^e with 6 * 2^e >= the block's largest
+ *     magnitude, e in [-127, 127]), no tensor scale.  Scale buffers keep one
+ *     byte per 16-element slot in either layout, each 32-element block's
+ *     code in both of its slots, so their sizes are those of NVFP4; amax
+ *     holds {0, 1, 1}.
+ */
+typedef enum { NVFP4_FORMAT_NVFP4 = 0, NVFP4_FORMAT_MXFP4 = 1 } nvfp4_format;
 typedef enum { NVFP4_RTN = 0, NVFP4_SR = 1 } nvfp4_round;
 
 /*
@@ -104,7 +119,7 @@ typedef struct {
     int64_t cols;
     int64_t ld_codes;
     int32_t scale_layout; /* nvfp4_scale_layout */
-    int32_t reserved;     /* must be 0 */
+    int32_t format;       /* nvfp4_format */
 } nvfp4_tensor;
 
 /* Bytes of the scale buffer of a [rows][cols] tensor in `scale_layout`
@@ -121,7 +136,12 @@ size_t nvfp4_workspace_size(void);
  * and the blog's micro-block / 2D-block / stochastic-rounding items.
  *   x            device, [rows][ldx] elements of `dtype` (ldx >= cols).
  *   block        1x16 (activations, gradients) or 16x16 (weights; RTN only,
- *                rows % 16 == 0).
+ *                rows % 16 == 0): NVFP4, outputs with format NVFP4.
+ *                MX1x32: MXFP4 (outputs with format MXFP4; RTN or SR;
+ *                cols % 32 == 0 for out_rowwise, rows % 32 == 0 for
+ *                out_colwise).  MXFP4 has no tensor amax, so it reads x once;
+ *                a 32-element block holding a NaN or an infinity flags
+ *                NVFP4_ERR_NONFINITE and gets zero codes and scale.
  *   round, seed  rounding mode and the Philox key for SR.
  *   out_rowwise  if non-NULL: describes x, [rows][cols], blocks along cols
  *                (cols % 16 == 0).
@@ -172,7 +192,10 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t
  * of word 0 of Philox4x32-10(key = rht_seed, counter = (0, 0, 1, 0)), the
  * butterfly evaluated stage by stage over index bits 0..3 in FP32.  Then the
  * tensor amax of y, and y^T is quantized with 1x16 blocks along the rows.
- *   out_colwise  describes y^T, [cols][rows]; rows % 16 == 0.
+ *   out_colwise  describes y^T, [cols][rows]; rows % 16 == 0.  Its format
+ *                selects the encoding: NVFP4 (1x16 blocks, the tensor amax
+ *                taken over y) or MXFP4 (1x32 blocks, rows % 32 == 0, no
+ *                amax pass).
  *   Other arguments as nvfp4_quantize.  Both Wgrad operands must use the
  *   same rht_seed so the transform cancels in the product.
  */
@@ -186,7 +209,10 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
  *               sum_{16} e2m1(A[m][k]) e2m1(B[n][k]),
  * a block-scaled FP4 GEMM on the tcgen05 tensor cores with FP32
  * accumulation (blog: Blackwell FP4 tensor cores run the linear layers).
- *   A            [M][K] quantized, B [N][K] quantized, both with
+ *   A            [M][K] quantized, B [N][K] quantized, both of the same
+ *                format (NVFP4: kind::mxf4nvf4, scale_vec::4X, E4M3 scales,
+ *                alpha = S_dec(A) S_dec(B); MXFP4: scale_vec::2X, UE8M0
+ *                scales, alpha = 1), both with
  *                NVFP4_SCALES_MMA scales (16-byte aligned buffers of
  *                nvfp4_scales_bytes() bytes), A->cols == B->cols == K,
  *                K % 64 == 0.

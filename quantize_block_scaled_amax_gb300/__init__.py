@@ -27,11 +27,13 @@ __all__ = [
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA = range(7)
 IN_BF16, IN_FP32 = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-BLOCK_1x16, BLOCK_16x16 = 0, 1
+BLOCK_1x16, BLOCK_16x16, BLOCK_MX1x32 = 0, 1, 2
+FORMAT_NVFP4, FORMAT_MXFP4 = 0, 1
 RTN, SR = 0, 1
 SCALES_LINEAR, SCALES_MMA = 0, 1
 
-_BLOCKS = {"1x16": BLOCK_1x16, "16x16": BLOCK_16x16}
+_BLOCKS = {"1x16": BLOCK_1x16, "16x16": BLOCK_16x16, "mx1x32": BLOCK_MX1x32}
+_FORMATS = {"nvfp4": FORMAT_NVFP4, "mxfp4": FORMAT_MXFP4}
 _ROUNDS = {"rtn": RTN, "sr": SR}
 _LAYOUTS = {"linear": SCALES_LINEAR, "mma": SCALES_MMA}
 
@@ -45,7 +47,7 @@ class NVFP4Error(RuntimeError):
 class nvfp4_tensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("amax", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld_codes", ctypes.c_int64),
-                ("scale_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("scale_layout", ctypes.c_int32), ("format", ctypes.c_int32)]
 
 
 class nvfp4_linear_ctx(ctypes.Structure):
@@ -133,17 +135,20 @@ def _workspace(device) -> torch.Tensor:
 
 
 class QTensor:
-    """A quantized NVFP4 tensor held in torch device buffers.
+    """A quantized tensor held in torch device buffers.
 
     codes  uint8 [rows][ld_codes] (two E2M1 codes per byte, low nibble first)
-    scales uint8 flat buffer, E4M3 block scales in ``scale_layout``
-    amax   float32 [3] = (A, S_dec, S_enc)
+    scales uint8 flat buffer of block scales in ``scale_layout``: E4M3 per 16
+           elements (fmt "nvfp4"), or UE8M0 per 32 elements stored in both of
+           the block's 16-element slots (fmt "mxfp4")
+    amax   float32 [3] = (A, S_dec, S_enc); (0, 1, 1) for "mxfp4"
     """
 
-    def __init__(self, codes, scales, amax, rows, cols, scale_layout):
+    def __init__(self, codes, scales, amax, rows, cols, scale_layout, fmt="nvfp4"):
         self.codes, self.scales, self.amax = codes, scales, amax
         self.rows, self.cols = int(rows), int(cols)
         self.scale_layout = scale_layout
+        self.fmt = fmt
 
     @property
     def ld_codes(self) -> int:
@@ -151,15 +156,15 @@ class QTensor:
 
     def c(self) -> nvfp4_tensor:
         return nvfp4_tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.amax.data_ptr(), self.rows,
-                            self.cols, self.ld_codes, _LAYOUTS[self.scale_layout], 0)
+                            self.cols, self.ld_codes, _LAYOUTS[self.scale_layout], _FORMATS[self.fmt])
 
 
-def empty_qtensor(rows: int, cols: int, device, scale_layout: str = "mma") -> QTensor:
+def empty_qtensor(rows: int, cols: int, device, scale_layout: str = "mma", fmt: str = "nvfp4") -> QTensor:
     ld = ((cols // 2 + 15) // 16) * 16
     codes = torch.empty(rows, ld, dtype=torch.uint8, device=device)
     scales = torch.empty(max(nvfp4_scales_bytes(rows, cols, scale_layout), 16), dtype=torch.uint8, device=device)
     amax = torch.empty(4, dtype=torch.float32, device=device)
-    return QTensor(codes, scales, amax, rows, cols, scale_layout)
+    return QTensor(codes, scales, amax, rows, cols, scale_layout, fmt)
 
 
 def _in_dtype(x: torch.Tensor) -> int:
@@ -180,13 +185,15 @@ def _check_input(x: torch.Tensor):
 def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", seed: int = 0, *,
                    rowwise: bool = True, colwise: bool = False, scale_layout: str = "mma",
                    out_rowwise: QTensor | None = None, out_colwise: QTensor | None = None, stream=None):
-    """Quantize x [rows][cols]; returns (rowwise QTensor or None, colwise QTensor or None)."""
+    """Quantize x [rows][cols]; returns (rowwise QTensor or None, colwise QTensor or None).
+    block "1x16" / "16x16" give NVFP4, "mx1x32" MXFP4."""
     _check_input(x)
     rows, cols = x.shape
+    fmt = "mxfp4" if block == "mx1x32" else "nvfp4"
     if rowwise and out_rowwise is None:
-        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout)
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout, fmt)
     if colwise and out_colwise is None:
-        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout, fmt)
     r = out_rowwise.c() if rowwise else None
     c = out_colwise.c() if colwise else None
     ws = _workspace(x.device)
@@ -205,10 +212,11 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, block: str = "1x16", round: str = "r
     of its own.  Pass preallocated outputs to allocate nothing here either."""
     _check_input(x)
     rows, cols = x.shape
+    fmt = "mxfp4" if block == "mx1x32" else "nvfp4"
     if rowwise and out_rowwise is None:
-        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout)
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout, fmt)
     if colwise and out_colwise is None:
-        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout, fmt)
     r = out_rowwise.c() if rowwise else None
     c = out_colwise.c() if colwise else None
     st = lib().nvfp4_quantize_noalloc(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _BLOCKS[block],
@@ -219,12 +227,15 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, block: str = "1x16", round: str = "r
 
 
 def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,
-                       scale_layout: str = "mma", out_colwise: QTensor | None = None, stream=None) -> QTensor:
-    """16-point RHT along the rows of x, then colwise 1x16 quantization of the result's transpose."""
+                       scale_layout: str = "mma", fmt: str = "nvfp4", out_colwise: QTensor | None = None,
+                       stream=None) -> QTensor:
+    """16-point RHT along the rows of x, then colwise quantization of the
+    result's transpose: 1x16 NVFP4 (fmt "nvfp4") or 1x32 MXFP4 ("mxfp4");
+    a given out_colwise decides by its own fmt."""
     _check_input(x)
     rows, cols = x.shape
     if out_colwise is None:
-        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout, fmt)
     c = out_colwise.c()
     ws = _workspace(x.device)
     st = lib().nvfp4_rht_quantize(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,

@@ -94,7 +94,8 @@ nvfp4_status check_out(const nvfp4_tensor* t, int64_t rows, int64_t cols, const 
                     (long long)t->ld_codes);
     if (t->scale_layout != NVFP4_SCALES_LINEAR && t->scale_layout != NVFP4_SCALES_MMA)
         return fail(NVFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, t->scale_layout);
-    if (t->reserved != 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: reserved field must be 0", name);
+    if (t->format != NVFP4_FORMAT_NVFP4 && t->format != NVFP4_FORMAT_MXFP4)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: bad format %d", name, t->format);
     if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->amax) & 3u))
         return fail(NVFP4_ERR_INVALID_ARG, "%s: codes/scales must be 16-byte aligned, amax 4-byte aligned", name);
     return NVFP4_OK;
@@ -181,8 +182,10 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
     g_err[0] = 0;
     nvfp4_status st = check_input(x, dtype, rows, cols, ldx);
     if (st) return st;
-    if (block != NVFP4_BLOCK_1x16 && block != NVFP4_BLOCK_16x16)
+    if (block != NVFP4_BLOCK_1x16 && block != NVFP4_BLOCK_16x16 && block != NVFP4_BLOCK_MX1x32)
         return fail(NVFP4_ERR_INVALID_ARG, "bad block %d", block);
+    const bool mx = block == NVFP4_BLOCK_MX1x32;
+    const int32_t fmt = mx ? NVFP4_FORMAT_MXFP4 : NVFP4_FORMAT_NVFP4;
     if (round != NVFP4_RTN && round != NVFP4_SR) return fail(NVFP4_ERR_INVALID_ARG, "bad round %d", round);
     if (!out_rowwise && !out_colwise) return fail(NVFP4_ERR_INVALID_ARG, "no output requested");
     if (out_rowwise && (st = check_out(out_rowwise, rows, cols, "out_rowwise"))) return st;
@@ -190,6 +193,10 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
         if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "colwise output needs rows %% 16 == 0");
         if ((st = check_out(out_colwise, cols, rows, "out_colwise"))) return st;
     }
+    if ((out_rowwise && out_rowwise->format != fmt) || (out_colwise && out_colwise->format != fmt))
+        return fail(NVFP4_ERR_INVALID_ARG, "output format must be %s for this block", mx ? "MXFP4" : "NVFP4");
+    if (mx && ((out_rowwise && cols % 32) || (out_colwise && rows % 32)))
+        return fail(NVFP4_ERR_INVALID_ARG, "MXFP4 needs 32-element blocks (cols %% 32 rowwise, rows %% 32 colwise)");
     if (block == NVFP4_BLOCK_16x16) {
         if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "16x16 blocks need rows %% 16 == 0");
         if (round != NVFP4_RTN) return fail(NVFP4_ERR_UNSUPPORTED, "16x16 blocks support RTN only");
@@ -205,9 +212,12 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
     if (out_rowwise && (st = zero_scale_padding(out_rowwise, s))) return st;
     if (out_colwise && (st = zero_scale_padding(out_colwise, s))) return st;
 
-    const int ag = amax_grid(rows, cols, ldx, fp32, dev->num_sms);
-    launch_amax(x, fp32, rows, cols, ldx, partials, ag, s);
-    if ((st = check_launch("amax"))) return st;
+    int ag = 0;
+    if (!mx) {  // MXFP4 has no tensor scale, hence no amax pass
+        ag = amax_grid(rows, cols, ldx, fp32, dev->num_sms);
+        launch_amax(x, fp32, rows, cols, ldx, partials, ag, s);
+        if ((st = check_launch("amax"))) return st;
+    }
 
     if (block == NVFP4_BLOCK_16x16) {
         const int g = cap_grid(tiles_2d(rows, cols), 8, dev->num_sms);
@@ -223,13 +233,14 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
         const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
         const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
         launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
-                                scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, seed, g, s);
+                                scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, mx, seed, g, s);
         if ((st = check_launch("quantize_rowwise"))) return st;
     }
     if (out_colwise) {
         const int g = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
         launch_quantize_colwise(x, fp32, rows, cols, ldx, partials, ag, out_colwise->codes, out_colwise->ld_codes,
-                                scale_out(*out_colwise), out_colwise->amax, dev->status, sr, seed, false, 0, g, s);
+                                scale_out(*out_colwise), out_colwise->amax, dev->status, sr, mx, seed, false, 0, g,
+                                s);
         if ((st = check_launch("quantize_colwise"))) return st;
     }
     return NVFP4_OK;
@@ -245,6 +256,8 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     if (!out_colwise) return fail(NVFP4_ERR_INVALID_ARG, "out_colwise is null");
     if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "RHT needs rows %% 16 == 0");
     if ((st = check_out(out_colwise, cols, rows, "out_colwise"))) return st;
+    const bool mx = out_colwise->format == NVFP4_FORMAT_MXFP4;
+    if (mx && rows % 32) return fail(NVFP4_ERR_INVALID_ARG, "MXFP4 needs rows %% 32 == 0");
     if ((st = check_workspace(workspace, workspace_bytes))) return st;
     DeviceInfo* dev;
     if ((st = device_info(&dev))) return st;
@@ -253,15 +266,18 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     const bool fp32 = dtype == NVFP4_IN_FP32;
     uint32_t* partials = static_cast<uint32_t*>(workspace);
     if ((st = zero_scale_padding(out_colwise, s))) return st;
-    const int64_t units = (rows / 16) * (cols / (fp32 ? 4 : 8));
-    const int ag = (int)std::max<int64_t>(
-        1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads), (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
-    launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
-    if ((st = check_launch("rht_amax"))) return st;
+    int ag = 0;
+    if (!mx) {
+        const int64_t units = (rows / 16) * (cols / (fp32 ? 4 : 8));
+        ag = (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads),
+                                                           (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
+        launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
+        if ((st = check_launch("rht_amax"))) return st;
+    }
     const int g = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
     launch_quantize_colwise(x, fp32, rows, cols, ldx, partials, ag, out_colwise->codes, out_colwise->ld_codes,
-                            scale_out(*out_colwise), out_colwise->amax, dev->status, round == NVFP4_SR, seed, true,
-                            rht_seed, g, s);
+                            scale_out(*out_colwise), out_colwise->amax, dev->status, round == NVFP4_SR, mx, seed,
+                            true, rht_seed, g, s);
     return check_launch("rht_quantize_colwise");
 }
 
@@ -281,6 +297,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
         return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands need NVFP4_SCALES_MMA scales");
     if (!aligned16(A->scales) || !aligned16(B->scales))
         return fail(NVFP4_ERR_INVALID_ARG, "GEMM scale buffers must be 16-byte aligned");
+    if (A->format != B->format) return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands must share one format");
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
         return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
     const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
@@ -303,6 +320,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     g.N = B->rows;
     g.K = A->cols;
     g.out_fp32 = out_dtype == NVFP4_OUT_FP32;
+    g.mx = A->format == NVFP4_FORMAT_MXFP4;
     g.status = dev->status;
     g.num_sms = dev->num_sms;
     const char* msg = nullptr;

@@ -168,10 +168,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1),
-// K-major both, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 7 at
-// bit 27, scale-factor data ids 0.
-__host__ __device__ constexpr uint32_t instr_desc_nvf4(int m, int n) {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 7) << 27);
+// K-major both, N >> 3 at bit 17, scale type at bit 23 (0 = UE4M3 for
+// NVFP4, 1 = UE8M0 for MXFP4), M >> 7 at bit 27, scale-factor data ids 0
+// (with scale_vec::2X the MMA reads bytes 0 and 1 of each scale word).
+__host__ __device__ constexpr uint32_t instr_desc_nvf4(int m, int n, bool ue8m0) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
+           ((uint32_t)(m >> 7) << 27);
 }
 
 __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -180,6 +182,18 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// MXFP4: two UE8M0 scales per row per K = 64 (32-element blocks).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
         "}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
@@ -249,6 +263,7 @@ struct Params {
     int n_katoms;             // atoms per 128-row group: 4 * ceil(K / 256)
     int b_groups;             // 128-row groups of B: ceil(N / 128)
     int out_fp32;
+    int mx;                   // MXFP4 operands (UE8M0 scales, 32-element blocks)
     uint32_t* status;
 };
 
@@ -311,7 +326,7 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
 __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
                                          uint32_t tmem_base) {
     const Sched S(p);
-    const uint32_t idesc = instr_desc_nvf4(BM, BN);
+    const uint32_t idesc = instr_desc_nvf4(BM, BN, p.mx != 0);
     const uint32_t sf_base = tmem_base + kAccCols;
     uint32_t it = 0, tc = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
@@ -330,7 +345,10 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
             for (int j = 0; j < kMmaPerStage; ++j) {
                 const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
                 const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
-                mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                if (p.mx)
+                    mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                else
+                    mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
             }
             mma_commit(&ss->empty[s]);
         }
@@ -373,6 +391,19 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
                 wb[0][j] = *reinterpret_cast<const uint4*>(sf + kSfRunBytes + j * kSfAtomBytes);
                 wb[1][j] = b_hi ? *reinterpret_cast<const uint4*>(sf + 2 * kSfRunBytes + j * kSfAtomBytes)
                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (p.mx) {
+                // MXFP4 stores each 32-element block's scale in both of its
+                // 16-element slots; scale_vec::2X wants the two blocks of an
+                // MMA in bytes 0 and 1 of the word
+#pragma unroll
+                for (int j = 0; j < kMmaPerStage; ++j) {
+                    wa[j] = __byte_perm(wa[j], 0u, 0x4420);
+                    wb[0][j] = make_uint4(__byte_perm(wb[0][j].x, 0u, 0x4420), __byte_perm(wb[0][j].y, 0u, 0x4420),
+                                          __byte_perm(wb[0][j].z, 0u, 0x4420), __byte_perm(wb[0][j].w, 0u, 0x4420));
+                    wb[1][j] = make_uint4(__byte_perm(wb[1][j].x, 0u, 0x4420), __byte_perm(wb[1][j].y, 0u, 0x4420),
+                                          __byte_perm(wb[1][j].z, 0u, 0x4420), __byte_perm(wb[1][j].w, 0u, 0x4420));
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ss->sf_free[s]);
@@ -636,6 +667,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.n_katoms = 4 * p.num_k;
     p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
+    p.mx = g.mx;
     p.status = g.status;
     // persistent: one CTA per SM, at most one per tile
     const int64_t tiles = (int64_t)p.num_m * p.num_n;

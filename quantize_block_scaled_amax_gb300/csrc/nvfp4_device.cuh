@@ -74,6 +74,28 @@ __device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc) {
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4 block scale (the format NVFP4 is compared against: paper summary
+// page, format paragraph; 32-element blocks, power-of-two UE8M0 scale, no
+// tensor scale): the smallest e with 6 * 2^e >= bamax, clamped to
+// [-127, 127], from the bits of bamax = 1.m * 2^(E-127): 6 * 2^e = 1.5 *
+// 2^(e+2) covers it at e = E - 129 when 1.m <= 1.5, else at e = E - 128; a
+// subnormal bamax (< 2^-126) is covered by the smallest scale.  Returns the
+// UE8M0 code e + 127 (0 for an all-zero block).
+__device__ __forceinline__ uint32_t mx_block_scale(float bamax) {
+    const uint32_t b = __float_as_uint(bamax);
+    const int E = (int)(b >> 23);
+    if (E == 0) return 0u;  // zero or subnormal: e = -127
+    int e = E - 129 + ((b & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    e = max(-127, min(127, e));
+    return (uint32_t)(e + 127);
+}
+
+// 2^-e for the UE8M0 code sb = e + 127 (exact; 2^-127 is an FP32 subnormal).
+__device__ __forceinline__ float mx_multiplier(uint32_t sb) {
+    return sb == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - sb) << 23);
+}
+
+// ---------------------------------------------------------------------------
 // E2M1 codes of values, two at a time: the hardware conversion rounds to
 // nearest (ties to even) and saturates to +-6; it keeps the sign of a value
 // that rounds to zero (code 0x8 for -0).  It places its first source operand

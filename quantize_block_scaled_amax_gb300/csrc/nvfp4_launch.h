@@ -23,11 +23,12 @@ void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64
                      uint32_t* partials, int grid, cudaStream_t s);
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, int grid, cudaStream_t s);
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, int grid,
+                             cudaStream_t s);
 void launch_quantize_colwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, bool rht, uint64_t rht_seed,
-                             int grid, cudaStream_t s);
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
+                             uint64_t rht_seed, int grid, cudaStream_t s);
 void launch_quantize_2d(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* partials,
                         int npartials, uint8_t* codes_r, int64_t ld_r, ScaleOut so_r, float* amax_r, uint8_t* codes_c,
                         int64_t ld_c, ScaleOut so_c, float* amax_c, uint32_t* status, int grid, cudaStream_t s);
@@ -48,6 +49,7 @@ struct GemmArgs {
     int64_t ldc;  // elements
     int64_t M, N, K;
     int out_fp32;
+    int mx;  // MXFP4 operands: UE8M0 scales per 32 elements, scale_vec::2X
     uint32_t* status;
     int num_sms;
 };

@@ -185,11 +185,12 @@ struct Block16 {
 #pragma unroll
         for (int k = 0; k < kVecs; ++k) raw[k] = __ldg(reinterpret_cast<const uint4*>(p) + k);
     }
-    __device__ __forceinline__ float absmax() const {
+    // bit pattern of the largest magnitude (>= 0x7f800000 for a NaN or an infinity)
+    __device__ __forceinline__ uint32_t absmax_bits() const {
         uint32_t m = 0;
 #pragma unroll
         for (int k = 0; k < kVecs; ++k) m = max(m, vec_absmax_bits<T>(raw[k]));
-        return __uint_as_float(m);
+        return m;
     }
     __device__ __forceinline__ void unpack(float v[16]) const {
 #pragma unroll
@@ -200,18 +201,50 @@ struct Block16 {
 };
 
 // ---------------------------------------------------------------------------
+// MXFP4 element encode of 16 values that share the UE8M0 scale sb of their
+// 32-element block (bmax_bits: the block's largest magnitude).  A block
+// holding a NaN or an infinity flags the status word and gets zero codes and
+// scale; an all-zero block gets zero codes and scale 0.
+template <bool kSR>
+__device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, uint64_t seed, uint64_t i0,
+                                             uint32_t* status, uint32_t& sb_out) {
+    if (bmax_bits >= 0x7f800000u) {
+        atomicOr(status, kStatusNonfinite);
+        sb_out = 0u;
+        return make_uint2(0u, 0u);
+    }
+    const uint32_t sb = mx_block_scale(__uint_as_float(bmax_bits));
+    sb_out = sb;
+    if (bmax_bits == 0u) return make_uint2(0u, 0u);
+    const float mul = mx_multiplier(sb);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], mul);
+    return encode16<kSR>(v, seed, i0);
+}
+
+// ---------------------------------------------------------------------------
 // Pass 2, rowwise 1x16.  A warp takes 64 consecutive blocks of one row (lane l
 // blocks l and l + 32: two coalesced 1 KB runs of bf16), loads both before
 // encoding either, and writes 8 bytes of codes and one scale byte per block.
 // Warp items run in the reverse of the amax pass's order, so the part of the
 // input read last by that pass (still in L2) is read first here.
-template <typename T, bool kSR>
+// kMX: MXFP4 instead (no amax pass, no tensor scale): a 32-element block is
+// the 16-blocks of lanes 2j and 2j+1, which exchange their block maxima; its
+// UE8M0 scale is written in both 16-block slots.
+template <typename T, bool kSR, bool kMX>
 __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantize_rowwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
     uint64_t seed) {
     __shared__ uint32_t red[33];
-    const TensorScales ts = reduce_partials(partials, npartials, amax_out, status, red);
+    TensorScales ts{};
+    if constexpr (!kMX) {
+        ts = reduce_partials(partials, npartials, amax_out, status, red);
+    } else if (blockIdx.x == 0 && threadIdx.x == 0) {
+        amax_out[0] = 0.0f;  // MXFP4 has no tensor scale
+        amax_out[1] = 1.0f;
+        amax_out[2] = 1.0f;
+    }
     const int lane = threadIdx.x & 31;
     const int64_t bpr = cols / 16;
     const int64_t ipr = (bpr + kRowItemBlocks - 1) / kRowItemBlocks;
@@ -228,22 +261,37 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
             ok[h] = kb0 + 32 * h < bpr;
             if (ok[h]) blk[h].load(x + r * ldx + (kb0 + 32 * h) * 16);
         }
+        uint32_t bm[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            bm[h] = ok[h] ? blk[h].absmax_bits() : 0u;
+            if constexpr (kMX) bm[h] = max(bm[h], __shfl_xor_sync(0xFFFFFFFFu, bm[h], 1));
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             if (!ok[h]) continue;
             const int64_t kb = kb0 + 32 * h;
-            BlockScale bs = block_scale(blk[h].absmax(), ts.s_enc);
-            if (!ts.finite) bs.sb = 0u;
+            const uint64_t i0 = (uint64_t)r * (uint64_t)cols + (uint64_t)kb * 16;
             uint2 c = make_uint2(0u, 0u);
-            if (bs.sb != 0u) {
+            uint32_t sb;
+            if constexpr (kMX) {
                 float v[16];
                 blk[h].unpack(v);
+                c = mx_encode16<kSR>(v, bm[h], seed, i0, status, sb);
+            } else {
+                BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc);
+                if (!ts.finite) bs.sb = 0u;
+                sb = bs.sb;
+                if (bs.sb != 0u) {
+                    float v[16];
+                    blk[h].unpack(v);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
-                c = encode16<kSR>(v, seed, (uint64_t)r * (uint64_t)cols + (uint64_t)kb * 16);
+                    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
+                    c = encode16<kSR>(v, seed, i0);
+                }
             }
             *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
-            so.p[so.offset(r, kb)] = (uint8_t)bs.sb;
+            so.p[so.offset(r, kb)] = (uint8_t)sb;
         }
     }
 }
@@ -256,14 +304,21 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
 constexpr int kColTileRows = 128;
 constexpr int kColTileCols = 64;
 
-template <typename T, bool kSR, bool kRHT>
+template <typename T, bool kSR, bool kRHT, bool kMX>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
     uint64_t seed, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
     __shared__ __align__(16) T tile[kColTileRows][kColTileCols];
-    const TensorScales ts = reduce_partials(partials, npartials, amax_out, status, red);
+    TensorScales ts{};
+    if constexpr (!kMX) {
+        ts = reduce_partials(partials, npartials, amax_out, status, red);
+    } else if (blockIdx.x == 0 && threadIdx.x == 0) {
+        amax_out[0] = 0.0f;  // MXFP4 has no tensor scale
+        amax_out[1] = 1.0f;
+        amax_out[2] = 1.0f;
+    }
     const uint32_t dmask = kRHT ? rht_sign_mask(rht_seed) : 0u;
 
     constexpr int V = 16 / sizeof(T);
@@ -295,27 +350,55 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
             uint32_t w[8];
             uint32_t sbs = 0;
             int nb = 0;
+            auto load_chunk = [&](int b, float v[16]) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                w[2 * b] = 0u;
-                w[2 * b + 1] = 0u;
-                if (orow0 + 16 * b < rows) {
-                    float v[16];
+                for (int i = 0; i < 16; ++i) {
+                    T e = tile[64 * half + 16 * b + i][col];
+                    if constexpr (sizeof(T) == 2)
+                        v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&e));
+                    else
+                        v[i] = *reinterpret_cast<const float*>(&e);
+                }
+                if constexpr (kRHT) rht16(v, dmask);
+            };
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        T e = tile[64 * half + 16 * b + i][col];
-                        if constexpr (sizeof(T) == 2)
-                            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&e));
-                        else
-                            v[i] = *reinterpret_cast<const float*>(&e);
+            for (int b = 0; b < 8; ++b) w[b] = 0u;
+            if constexpr (kMX) {
+                // two 32-element blocks (chunk pairs 0-1 and 2-3); rows % 32 == 0
+#pragma unroll
+                for (int pb = 0; pb < 2; ++pb) {
+                    if (orow0 + 32 * pb < rows) {
+                        float v0[16], v1[16];
+                        load_chunk(2 * pb, v0);
+                        load_chunk(2 * pb + 1, v1);
+                        uint32_t bm = 0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) bm = max(bm, max(abs_bits(v0[i]), abs_bits(v1[i])));
+                        const uint64_t i0 = (uint64_t)oc * (uint64_t)rows + orow0 + 32 * pb;
+                        uint32_t sb;
+                        const uint2 c0 = mx_encode16<kSR>(v0, bm, seed, i0, status, sb);
+                        const uint2 c1 = mx_encode16<kSR>(v1, bm, seed, i0 + 16, status, sb);
+                        w[4 * pb] = c0.x;
+                        w[4 * pb + 1] = c0.y;
+                        w[4 * pb + 2] = c1.x;
+                        w[4 * pb + 3] = c1.y;
+                        sbs |= (sb | (sb << 8)) << (16 * pb);
+                        nb = 2 * pb + 2;
                     }
-                    if constexpr (kRHT) rht16(v, dmask);
-                    uint32_t sb;
-                    uint2 c = quantize_block<kSR>(v, ts, seed, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
-                    w[2 * b] = c.x;
-                    w[2 * b + 1] = c.y;
-                    sbs |= sb << (8 * b);
-                    nb = b + 1;
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if (orow0 + 16 * b < rows) {
+                        float v[16];
+                        load_chunk(b, v);
+                        uint32_t sb;
+                        uint2 c = quantize_block<kSR>(v, ts, seed, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
+                        w[2 * b] = c.x;
+                        w[2 * b + 1] = c.y;
+                        sbs |= sb << (8 * b);
+                        nb = b + 1;
+                    }
                 }
             }
             if (nb > 0) {
@@ -486,34 +569,42 @@ void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64
 
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, int grid, cudaStream_t s) {
-#define NVFP4_ROW(T, SR)                                                                                    \
-    quantize_rowwise_kernel<T, SR><<<grid, kQuantThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx, \
-                                                                  partials, npartials, codes, ld_codes, so, \
-                                                                  amax_out, status, seed)
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, int grid,
+                             cudaStream_t s) {
+#define NVFP4_ROW(T, SR, MX)                                                                                    \
+    quantize_rowwise_kernel<T, SR, MX><<<grid, kQuantThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx, \
+                                                                      partials, npartials, codes, ld_codes, so, \
+                                                                      amax_out, status, seed)
+#define NVFP4_ROW_MX(T, SR) \
+    if (mx) NVFP4_ROW(T, SR, true); else NVFP4_ROW(T, SR, false)
     if (fp32) {
-        if (sr) NVFP4_ROW(float, true); else NVFP4_ROW(float, false);
+        if (sr) { NVFP4_ROW_MX(float, true); } else { NVFP4_ROW_MX(float, false); }
     } else {
-        if (sr) NVFP4_ROW(__nv_bfloat16, true); else NVFP4_ROW(__nv_bfloat16, false);
+        if (sr) { NVFP4_ROW_MX(__nv_bfloat16, true); } else { NVFP4_ROW_MX(__nv_bfloat16, false); }
     }
+#undef NVFP4_ROW_MX
 #undef NVFP4_ROW
 }
 
 void launch_quantize_colwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, uint64_t seed, bool rht, uint64_t rht_seed,
-                             int grid, cudaStream_t s) {
-#define NVFP4_COL(T, SR, RHT)                                                                                    \
-    quantize_colwise_kernel<T, SR, RHT><<<grid, kColThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx,  \
-                                                                     partials, npartials, codes, ld_codes, so,   \
-                                                                     amax_out, status, seed, rht_seed)
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
+                             uint64_t rht_seed, int grid, cudaStream_t s) {
+#define NVFP4_COL(T, SR, RHT, MX)                                                                                    \
+    quantize_colwise_kernel<T, SR, RHT, MX><<<grid, kColThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx,  \
+                                                                         partials, npartials, codes, ld_codes, so,   \
+                                                                         amax_out, status, seed, rht_seed)
+#define NVFP4_COL_MX(T, SR, RHT) \
+    if (mx) NVFP4_COL(T, SR, RHT, true); else NVFP4_COL(T, SR, RHT, false)
+#define NVFP4_COL_RHT(T, SR) \
+    if (rht) { NVFP4_COL_MX(T, SR, true); } else { NVFP4_COL_MX(T, SR, false); }
     if (fp32) {
-        if (sr) { if (rht) NVFP4_COL(float, true, true); else NVFP4_COL(float, true, false); }
-        else    { if (rht) NVFP4_COL(float, false, true); else NVFP4_COL(float, false, false); }
+        if (sr) { NVFP4_COL_RHT(float, true) } else { NVFP4_COL_RHT(float, false) }
     } else {
-        if (sr) { if (rht) NVFP4_COL(__nv_bfloat16, true, true); else NVFP4_COL(__nv_bfloat16, true, false); }
-        else    { if (rht) NVFP4_COL(__nv_bfloat16, false, true); else NVFP4_COL(__nv_bfloat16, false, false); }
+        if (sr) { NVFP4_COL_RHT(__nv_bfloat16, true) } else { NVFP4_COL_RHT(__nv_bfloat16, false) }
     }
+#undef NVFP4_COL_RHT
+#undef NVFP4_COL_MX
 #undef NVFP4_COL
 }
 

@@ -1,0 +1,132 @@
+"""``torch.autograd`` wrapper of the NVFP4 linear layer Y = X W^T.
+
+The forward and backward passes are the C ABI's ``nvfp4_linear_fwd`` and
+``nvfp4_linear_bwd`` (through the binding): X 1x16 RTN, W 16x16 RTN in both
+layouts, Y in bf16; dY 1x16 SR for Dgrad, and the 16-point RHT along the
+tokens with SR on dY and RTN on X for Wgrad (paper page "Pretraining Large
+Language Models with NVFP4", recipe paragraph; blog "NVFP4 Trains with
+Precision of 16-Bit...", technique list).  Nothing here computes: the module
+keeps the caller-side state the C calls need (quantized-operand buffers per
+shape and device, and the random seeds).
+
+Seeds: every backward pass draws a fresh stochastic-rounding seed from a
+counter (``seed_base + call index``), so repeated steps do not reuse the
+rounding decisions, and a run started from the same ``seed_base`` repeats
+them exactly.  The RHT sign vector uses ``rht_seed`` (one per layer; both
+Wgrad operands of a call share it, as the transform requires).
+"""
+from __future__ import annotations
+
+import threading
+
+import torch
+
+from . import LinearContext, nvfp4_linear_bwd, nvfp4_linear_fwd
+
+__all__ = ["NVFP4LinearFunction", "NVFP4Linear", "nvfp4_linear"]
+
+
+class _SeedCounter:
+    def __init__(self, base: int):
+        self._next = int(base)
+        self._lock = threading.Lock()
+
+    def take(self) -> int:
+        with self._lock:
+            s = self._next
+            self._next += 1
+            return s & 0xFFFFFFFFFFFFFFFF
+
+
+class _Contexts:
+    """Quantized-operand buffers, one set per (M, N, K, device)."""
+
+    def __init__(self):
+        self._ctx = {}
+        self._lock = threading.Lock()
+
+    def get(self, m: int, n: int, k: int, device) -> LinearContext:
+        key = (m, n, k, str(device))
+        with self._lock:
+            c = self._ctx.get(key)
+            if c is None:
+                c = LinearContext(m, n, k, device)
+                self._ctx[key] = c
+            return c
+
+
+def _check_shapes(x2: torch.Tensor, w: torch.Tensor) -> None:
+    if x2.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError(f"NVFP4 linear takes bf16 X and W, got {x2.dtype} and {w.dtype}")
+    if w.dim() != 2 or x2.shape[1] != w.shape[1]:
+        raise ValueError(f"X [..., K] and W [N, K] disagree: {tuple(x2.shape)} vs {tuple(w.shape)}")
+    m, k = x2.shape
+    n = w.shape[0]
+    if m % 64 or n % 64 or k % 64 or m == 0 or n == 0 or k == 0:
+        raise ValueError(f"M, N, K must be positive multiples of 64, got M={m} N={n} K={k}")
+    if not x2.is_cuda or not w.is_cuda or x2.device != w.device:
+        raise ValueError("X and W must be CUDA tensors on the same device")
+
+
+class NVFP4LinearFunction(torch.autograd.Function):
+    """Y = X W^T with the NVFP4 recipe; X [..., K] bf16, W [N, K] bf16.
+
+    Returns Y [..., N] bf16.  Gradients: dX bf16, dW in W's dtype (the Wgrad
+    GEMM accumulates and writes FP32; the cast to bf16 is the one rounding
+    this wrapper adds)."""
+
+    @staticmethod
+    def forward(ctx, x, w, contexts: _Contexts, seeds: _SeedCounter, rht_seed: int):
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        w = w.contiguous()
+        _check_shapes(x2, w)
+        m, k = x2.shape
+        n = w.shape[0]
+        lc = contexts.get(m, n, k, x2.device)
+        y = nvfp4_linear_fwd(x2, w, lc)
+        ctx.save_for_backward(x2)
+        ctx.lc = lc
+        ctx.lead = lead
+        ctx.seeds = seeds
+        ctx.rht_seed = rht_seed
+        ctx.w_dtype = w.dtype
+        return y.reshape(*lead, n)
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x2,) = ctx.saved_tensors
+        lc = ctx.lc
+        dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
+        dx, dw = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed)
+        # linear_fwd quantized W into lc.wtq, which Dgrad reads; a later forward
+        # through the same context must not run before this backward is done,
+        # which the stream order guarantees for single-stream training.
+        return dx.reshape(*ctx.lead, lc.K), dw.to(ctx.w_dtype), None, None, None
+
+
+class NVFP4Linear(torch.nn.Module):
+    """A bias-free linear layer whose three GEMMs run in NVFP4 on the tcgen05
+    tensor cores.  ``weight`` is a bf16 parameter [out_features, in_features]
+    (the high-precision master copy stays with the optimizer, as in the
+    recipe); in_features, out_features and the token count must be multiples
+    of 64."""
+
+    def __init__(self, in_features: int, out_features: int, device=None, seed_base: int = 1, rht_seed: int = 2):
+        super().__init__()
+        if in_features % 64 or out_features % 64:
+            raise ValueError("in_features and out_features must be multiples of 64")
+        self.weight = torch.nn.Parameter(torch.empty(out_features, in_features, dtype=torch.bfloat16, device=device))
+        torch.nn.init.normal_(self.weight, std=0.02)
+        self._contexts = _Contexts()
+        self._seeds = _SeedCounter(seed_base)
+        self.rht_seed = int(rht_seed)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return NVFP4LinearFunction.apply(x, self.weight, self._contexts, self._seeds, self.rht_seed)
+
+
+def nvfp4_linear(x: torch.Tensor, w: torch.Tensor, sr_seed: int = 1, rht_seed: int = 2) -> torch.Tensor:
+    """Functional form with a fixed stochastic-rounding seed (every backward
+    of this call uses ``sr_seed``)."""
+    return NVFP4LinearFunction.apply(x, w, _Contexts(), _SeedCounter(sr_seed), int(rht_seed))

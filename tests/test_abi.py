@@ -85,6 +85,13 @@ def test_host_argument_checks_need_no_gpu(L):
     # workspace too small
     assert L.nvfp4_quantize(16, 0, 16, 32, 32, 0, 0, 0, ctypes.byref(t), None, 16, 64, None) == q.ERR_WORKSPACE
     assert b"workspace" in L.nvfp4_last_error()
+    # MXFP4: 32-element blocks, and outputs of the MXFP4 format
+    tm = q.nvfp4_tensor(16, 16, 16, 16, 48, 32, 1, 1)
+    assert L.nvfp4_quantize(16, 0, 16, 48, 48, 2, 0, 0, ctypes.byref(tm), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    tm = q.nvfp4_tensor(16, 16, 16, 16, 64, 32, 1, 0)      # NVFP4-format output for an MX block
+    assert L.nvfp4_quantize(16, 0, 16, 64, 64, 2, 0, 0, ctypes.byref(tm), None, 16, 8192, None) == q.ERR_INVALID_ARG
+    tm = q.nvfp4_tensor(16, 16, 16, 16, 64, 32, 1, 7)      # unknown format
+    assert L.nvfp4_quantize(16, 0, 16, 64, 64, 0, 0, 0, ctypes.byref(tm), None, 16, 8192, None) == q.ERR_INVALID_ARG
     # RHT needs rows % 16 == 0
     tc2 = q.nvfp4_tensor(16, 16, 16, 32, 24, 16, 1, 0)
     assert L.nvfp4_rht_quantize(16, 0, 24, 32, 32, 0, 0, 0, ctypes.byref(tc2), 16, 8192, None) == q.ERR_INVALID_ARG
@@ -98,6 +105,8 @@ def test_gemm_argument_checks_need_no_gpu(L):
     b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 0, 0)     # row-major (LINEAR) scales
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
     b = q.nvfp4_tensor(16, 24, 16, 64, 128, 64, 1, 0)     # scale buffer not 16-byte aligned
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
+    b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 1, 1)     # MXFP4 B with an NVFP4 A
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
     a = q.nvfp4_tensor(16, 16, 16, 128, 96, 48, 1, 0)     # K % 64 != 0
     b = q.nvfp4_tensor(16, 16, 16, 64, 96, 48, 1, 0)
