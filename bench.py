@@ -272,6 +272,8 @@ def gpu_bench(args):
     if st != nv.OK:
         raise RuntimeError(f"device status {st} after the timed region")
 
+    mx = None if args.no_mx else mx_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -322,6 +324,7 @@ def gpu_bench(args):
         "kernels": kernels,
         "share": {"gemm": round(gemm_ms / (gemm_ms + quant_ms), 4), "quantize": round(quant_ms / (gemm_ms + quant_ms), 4)},
         "gpu_launches": args.steps * sum(launches_per_op.values()),
+        "mxfp4": mx,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -432,6 +435,72 @@ def reference_arm(args):
     }
 
 
+def mx_measure(nv, x, w, dy, flush, stream, steps):
+    """The same layer step with MXFP4 operands (32-element blocks, UE8M0
+    scales, no tensor scale: one read per quantize; weights 1x32 in both
+    layouts, there being no 2D MXFP4 block), timed op by op like the main
+    step.  Not part of `value`."""
+    import torch
+    import workloads
+    dev = x.device
+    q = {name: nv.empty_qtensor(r, c, dev, fmt="mxfp4") for name, (r, c) in
+         dict(xq=(M, K), wq=(N, K), wtq=(K, N), dyq=(M, N), dytq=(N, M), xtq=(K, M)).items()}
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    ops = [
+        ("quant_x_mx_rtn", lambda: nv.nvfp4_quantize(x, block="mx1x32", out_rowwise=q["xq"])),
+        ("quant_w_mx_both", lambda: nv.nvfp4_quantize(w, block="mx1x32", colwise=True, out_rowwise=q["wq"],
+                                                      out_colwise=q["wtq"])),
+        ("gemm_fprop_mx", lambda: nv.nvfp4_gemm(q["xq"], q["wq"], out=y)),
+        ("quant_dy_mx_sr", lambda: nv.nvfp4_quantize(dy, block="mx1x32", round="sr", seed=sr, out_rowwise=q["dyq"])),
+        ("gemm_dgrad_mx", lambda: nv.nvfp4_gemm(q["dyq"], q["wtq"], out=dx)),
+        ("rht_quant_dy_mx_sr", lambda: nv.nvfp4_rht_quantize(dy, round="sr", seed=sr, rht_seed=rh,
+                                                             out_colwise=q["dytq"])),
+        ("rht_quant_x_mx_rtn", lambda: nv.nvfp4_rht_quantize(x, rht_seed=rh, out_colwise=q["xtq"])),
+        ("gemm_wgrad_mx", lambda: nv.nvfp4_gemm(q["dytq"], q["xtq"], out=dw)),
+    ]
+    # algorithmic bytes: one read of the input, codes, one UE8M0 byte per 32 elements per layout
+    bx, bw, bdy = M * K * 2, N * K * 2, M * N * 2
+    nbytes = {"quant_x_mx_rtn": bx + M * K // 2 + M * K // 32,
+              "quant_w_mx_both": bw + 2 * (N * K // 2 + N * K // 32),
+              "quant_dy_mx_sr": bdy + M * N // 2 + M * N // 32,
+              "rht_quant_dy_mx_sr": bdy + M * N // 2 + M * N // 32,
+              "rht_quant_x_mx_rtn": bx + M * K // 2 + M * K // 32}
+    for _ in range(3):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize()
+    per = {name: 0.0 for name, _ in ops}
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(steps)]
+    for st in range(steps):
+        flush.fill_(st & 0xFF)
+        for (name, fn), (e0, e1) in zip(ops, evs[st]):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    for st in range(steps):
+        for (name, _), (e0, e1) in zip(ops, evs[st]):
+            per[name] += e0.elapsed_time(e1)
+    status = nv.nvfp4_sync_status()
+    if status != nv.OK:
+        raise RuntimeError(f"device status {status} after the MXFP4 step")
+    out = {}
+    for name, tot in per.items():
+        ms = tot / steps
+        if name.startswith("gemm"):
+            out[name] = {"ms": round(ms, 4), "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}
+        else:
+            out[name] = {"ms": round(ms, 4), "gbs": round(nbytes[name] / (ms * 1e-3) / 1e9, 1)}
+    step_ms = sum(per.values()) / steps
+    return {"ms_per_step": round(step_ms, 4), "tflops": round(3 * 2.0 * M * N * K / (step_ms * 1e-3) / 1e12, 2),
+            "steps": steps, "kernels": out,
+            "note": "same layer step with MXFP4 operands (1x32 UE8M0 blocks, no tensor scale, no amax pass)"}
+
+
 def profile_case(args):
     """One launch of one op of the step, for profiler captures: setup (input
     generation, quantization of the operands) runs first, then the op once."""
@@ -487,6 +556,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison step")
     ap.add_argument("--cpu-baseline-only", action="store_true")
     ap.add_argument("--cpu-sample-m", type=int, default=512)
     ap.add_argument("--cpu-sample-n", type=int, default=4096)
