@@ -273,6 +273,7 @@ def gpu_bench(args):
         raise RuntimeError(f"device status {st} after the timed region")
 
     mx = None if args.no_mx else mx_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
+    rht_rows = None if args.no_mx else rht_rows_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
 
     if rank != 0:
         if world > 1:
@@ -325,6 +326,7 @@ def gpu_bench(args):
         "share": {"gemm": round(gemm_ms / (gemm_ms + quant_ms), 4), "quantize": round(quant_ms / (gemm_ms + quant_ms), 4)},
         "gpu_launches": args.steps * sum(launches_per_op.values()),
         "mxfp4": mx,
+        "rht_fprop_dgrad_quantize": rht_rows,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -435,6 +437,59 @@ def reference_arm(args):
     }
 
 
+def _time_ops(nv, ops, flush, stream, steps):
+    """Total CUDA-event milliseconds of each op over `steps` passes (3
+    untimed warm-up passes; L2 flushed by a write before every pass)."""
+    import torch
+    for _ in range(3):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize()
+    per = {name: 0.0 for name, _ in ops}
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(steps)]
+    for st in range(steps):
+        flush.fill_(st & 0xFF)
+        for (name, fn), (e0, e1) in zip(ops, evs[st]):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    for st in range(steps):
+        for (name, _), (e0, e1) in zip(ops, evs[st]):
+            per[name] += e0.elapsed_time(e1)
+    status = nv.nvfp4_sync_status()
+    if status != nv.OK:
+        raise RuntimeError(f"device status {status} after timing {[n for n, _ in ops]}")
+    return per
+
+
+def rht_rows_measure(nv, x, w, dy, flush, stream, steps):
+    """Quantization of the Fprop and Dgrad operands with the 16-point RHT
+    along their K (the transform the pages leave optional there): X and W
+    rowwise RTN, dY rowwise SR, W^T colwise RTN.  Not part of `value`."""
+    import workloads
+    dev = x.device
+    from quantize_block_scaled_amax_gb300 import empty_qtensor
+    q = {name: empty_qtensor(r, c, dev) for name, (r, c) in
+         dict(xq=(M, K), wq=(N, K), wtq=(K, N), dyq=(M, N)).items()}
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    ops = [
+        ("rht_rows_x_rtn", lambda: nv.nvfp4_rht_quantize_rowwise(x, rht_seed=rh, out_rowwise=q["xq"])),
+        ("rht_rows_w_rtn", lambda: nv.nvfp4_rht_quantize_rowwise(w, rht_seed=rh, out_rowwise=q["wq"])),
+        ("rht_cols_w_rtn", lambda: nv.nvfp4_rht_quantize(w, rht_seed=rh, out_colwise=q["wtq"])),
+        ("rht_rows_dy_sr", lambda: nv.nvfp4_rht_quantize_rowwise(dy, round="sr", seed=sr, rht_seed=rh,
+                                                                 out_rowwise=q["dyq"])),
+    ]
+    bx, bw, bdy = M * K * 2, N * K * 2, M * N * 2
+    nbytes = {"rht_rows_x_rtn": 2 * bx + M * K // 2 + M * K // 16, "rht_rows_w_rtn": 2 * bw + N * K // 2 + N * K // 16,
+              "rht_cols_w_rtn": 2 * bw + N * K // 2 + N * K // 16,
+              "rht_rows_dy_sr": 2 * bdy + M * N // 2 + M * N // 16}
+    per = _time_ops(nv, ops, flush, stream, steps)
+    return {name: {"ms": round(t / steps, 4), "gbs": round(nbytes[name] / (t / steps * 1e-3) / 1e9, 1)}
+            for name, t in per.items()}
+
+
 def mx_measure(nv, x, w, dy, flush, stream, steps):
     """The same layer step with MXFP4 operands (32-element blocks, UE8M0
     scales, no tensor scale: one read per quantize; weights 1x32 in both
@@ -468,26 +523,7 @@ def mx_measure(nv, x, w, dy, flush, stream, steps):
               "quant_dy_mx_sr": bdy + M * N // 2 + M * N // 32,
               "rht_quant_dy_mx_sr": bdy + M * N // 2 + M * N // 32,
               "rht_quant_x_mx_rtn": bx + M * K // 2 + M * K // 32}
-    for _ in range(3):
-        for _, fn in ops:
-            fn()
-    torch.cuda.synchronize()
-    per = {name: 0.0 for name, _ in ops}
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-           for _ in range(steps)]
-    for st in range(steps):
-        flush.fill_(st & 0xFF)
-        for (name, fn), (e0, e1) in zip(ops, evs[st]):
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-    torch.cuda.synchronize()
-    for st in range(steps):
-        for (name, _), (e0, e1) in zip(ops, evs[st]):
-            per[name] += e0.elapsed_time(e1)
-    status = nv.nvfp4_sync_status()
-    if status != nv.OK:
-        raise RuntimeError(f"device status {status} after the MXFP4 step")
+    per = _time_ops(nv, ops, flush, stream, steps)
     out = {}
     for name, tot in per.items():
         ms = tot / steps
@@ -556,7 +592,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison step")
+    ap.add_argument("--no-mx", action="store_true",
+                    help="skip the MXFP4 comparison step and the RHT-on-Fprop/Dgrad quantize timings")
     ap.add_argument("--cpu-baseline-only", action="store_true")
     ap.add_argument("--cpu-sample-m", type=int, default=512)
     ap.add_argument("--cpu-sample-n", type=int, default=4096)

@@ -205,6 +205,23 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
                                 nvfp4_stream_t stream);
 
 /*
+ * nvfp4_rht_quantize_rowwise -- the 16-point RHT along each row (the GEMM's
+ * K for a rowwise operand: each 1x16 block is one transform chunk), then the
+ * tensor amax of the result and rowwise quantization.  The paper page allows
+ * the transform on the Fprop and Dgrad inputs too (limitations paragraph:
+ * applied to Wgrad only, its effect on the other GEMMs at larger scale left
+ * open); both operands of a GEMM transformed with the same rht_seed give the
+ * untransformed product, since (1/4) H16 is orthogonal.
+ *   out_rowwise  describes y, [rows][cols]; its format selects NVFP4 (1x16)
+ *                or MXFP4 (1x32, cols % 32 == 0, no amax pass).
+ *   Other arguments as nvfp4_quantize; the transform as nvfp4_rht_quantize.
+ */
+nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                        nvfp4_round round, uint64_t seed, uint64_t rht_seed,
+                                        const nvfp4_tensor* out_rowwise, void* workspace, size_t workspace_bytes,
+                                        nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm -- C[m][n] = S_dec(A) S_dec(B) sum_kb sbA[m][kb] sbB[n][kb]
  *               sum_{16} e2m1(A[m][k]) e2m1(B[n][k]),
  * a block-scaled FP4 GEMM on the tcgen05 tensor cores with FP32

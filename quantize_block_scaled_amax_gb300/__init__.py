@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
-    "nvfp4_quantize_noalloc", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_quantize_noalloc", "nvfp4_rht_quantize_rowwise", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
 
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_quantize_noalloc.argtypes = [vp, st, i64, i64, i64, st, st, u64, tp, tp, vp]
             L.nvfp4_rht_quantize.restype = st
             L.nvfp4_rht_quantize.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t, vp]
+            L.nvfp4_rht_quantize_rowwise.restype = st
+            L.nvfp4_rht_quantize_rowwise.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t,
+                                                     vp]
             L.nvfp4_gemm.restype = st
             L.nvfp4_gemm.argtypes = [tp, tp, vp, st, i64, vp, ctypes.c_size_t, vp]
             L.nvfp4_linear_fwd.restype = st
@@ -242,6 +245,23 @@ def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_s
                                   rht_seed, ctypes.byref(c), ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "nvfp4_rht_quantize")
     return out_colwise
+
+
+def nvfp4_rht_quantize_rowwise(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,
+                               scale_layout: str = "mma", fmt: str = "nvfp4", out_rowwise: QTensor | None = None,
+                               stream=None) -> QTensor:
+    """16-point RHT along the columns of each row of x (in 16-element chunks),
+    then rowwise quantization of the result: 1x16 NVFP4 or 1x32 MXFP4."""
+    _check_input(x)
+    rows, cols = x.shape
+    if out_rowwise is None:
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout, fmt)
+    r = out_rowwise.c()
+    ws = _workspace(x.device)
+    st = lib().nvfp4_rht_quantize_rowwise(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
+                                          rht_seed, ctypes.byref(r), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "nvfp4_rht_quantize_rowwise")
+    return out_rowwise
 
 
 def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,

@@ -233,7 +233,8 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
         const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
         const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
         launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
-                                scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, mx, seed, g, s);
+                                scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, mx, seed, false, 0, g,
+                                s);
         if ((st = check_launch("quantize_rowwise"))) return st;
     }
     if (out_colwise) {
@@ -279,6 +280,41 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
                             scale_out(*out_colwise), out_colwise->amax, dev->status, round == NVFP4_SR, mx, seed,
                             true, rht_seed, g, s);
     return check_launch("rht_quantize_colwise");
+}
+
+nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                        nvfp4_round round, uint64_t seed, uint64_t rht_seed,
+                                        const nvfp4_tensor* out_rowwise, void* workspace, size_t workspace_bytes,
+                                        nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    nvfp4_status st = check_input(x, dtype, rows, cols, ldx);
+    if (st) return st;
+    if (round != NVFP4_RTN && round != NVFP4_SR) return fail(NVFP4_ERR_INVALID_ARG, "bad round %d", round);
+    if (!out_rowwise) return fail(NVFP4_ERR_INVALID_ARG, "out_rowwise is null");
+    if ((st = check_out(out_rowwise, rows, cols, "out_rowwise"))) return st;
+    const bool mx = out_rowwise->format == NVFP4_FORMAT_MXFP4;
+    if (mx && cols % 32) return fail(NVFP4_ERR_INVALID_ARG, "MXFP4 needs cols %% 32 == 0");
+    if ((st = check_workspace(workspace, workspace_bytes))) return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev))) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool fp32 = dtype == NVFP4_IN_FP32;
+    uint32_t* partials = static_cast<uint32_t*>(workspace);
+    if ((st = zero_scale_padding(out_rowwise, s))) return st;
+    const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
+    int ag = 0;
+    if (!mx) {
+        ag = (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(items, (int64_t)kQuantThreads / 32),
+                                                           (int64_t)dev->num_sms * 8, (int64_t)kMaxPartials}));
+        launch_rht_rows_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
+        if ((st = check_launch("rht_rows_amax"))) return st;
+    }
+    const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
+    launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
+                            scale_out(*out_rowwise), out_rowwise->amax, dev->status, round == NVFP4_SR, mx, seed,
+                            true, rht_seed, g, s);
+    return check_launch("rht_quantize_rowwise");
 }
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,

@@ -23,8 +23,10 @@ void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64
                      uint32_t* partials, int grid, cudaStream_t s);
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, int grid,
-                             cudaStream_t s);
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
+                             uint64_t rht_seed, int grid, cudaStream_t s);
+void launch_rht_rows_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
+                          uint32_t* partials, int grid, cudaStream_t s);
 void launch_quantize_colwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
                              float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,

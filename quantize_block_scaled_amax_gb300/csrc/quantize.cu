@@ -158,6 +158,15 @@ __global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const T* __re
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
+// Pass 1 of the rowwise RHT path (the transform along each row, i.e. along
+// the GEMM's K of a rowwise operand): amax of the transformed tensor.  Warp
+// items as in the rowwise quantizer: 64 consecutive 16-element chunks of a
+// row, lane l taking chunks l and l + 32.
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads) rht_rows_amax_kernel(const T* __restrict__ x, int64_t rows,
+                                                                      int64_t cols, int64_t ldx, uint64_t rht_seed,
+                                                                      uint32_t* __restrict__ partials);
+
 // ---------------------------------------------------------------------------
 // Quantize one block of 16 values in place into 8 bytes of codes.
 template <bool kSR>
@@ -200,6 +209,42 @@ struct Block16 {
     }
 };
 
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads) rht_rows_amax_kernel(const T* __restrict__ x, int64_t rows,
+                                                                      int64_t cols, int64_t ldx, uint64_t rht_seed,
+                                                                      uint32_t* __restrict__ partials) {
+    __shared__ uint32_t red[33];
+    const uint32_t dmask = rht_sign_mask(rht_seed);
+    const int lane = threadIdx.x & 31;
+    const int64_t bpr = cols / 16;
+    const int64_t ipr = (bpr + kRowItemBlocks - 1) / kRowItemBlocks;
+    const int64_t nitems = rows * ipr;
+    const int64_t nwarps = (int64_t)gridDim.x * (kQuantThreads / 32);
+    uint32_t m = 0;
+    for (int64_t it = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5); it < nitems; it += nwarps) {
+        const int64_t r = it / ipr;
+        const int64_t kb0 = (it - r * ipr) * kRowItemBlocks + lane;
+        Block16<T> blk[2];
+        bool ok[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            ok[h] = kb0 + 32 * h < bpr;
+            if (ok[h]) blk[h].load(x + r * ldx + (kb0 + 32 * h) * 16);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ok[h]) continue;
+            float v[16];
+            blk[h].unpack(v);
+            rht16(v, dmask);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) m = max(m, abs_bits(v[k]));
+        }
+    }
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
 // ---------------------------------------------------------------------------
 // MXFP4 element encode of 16 values that share the UE8M0 scale sb of their
 // 32-element block (bmax_bits: the block's largest magnitude).  A block
@@ -231,11 +276,13 @@ __device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, ui
 // kMX: MXFP4 instead (no amax pass, no tensor scale): a 32-element block is
 // the 16-blocks of lanes 2j and 2j+1, which exchange their block maxima; its
 // UE8M0 scale is written in both 16-block slots.
-template <typename T, bool kSR, bool kMX>
+// kRHT: each 16-element block is first transformed by the 16-point RHT (the
+// block is the transform's chunk), and block maxima are taken afterwards.
+template <typename T, bool kSR, bool kMX, bool kRHT>
 __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantize_rowwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
-    uint64_t seed) {
+    uint64_t seed, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
     TensorScales ts{};
     if constexpr (!kMX) {
@@ -245,6 +292,7 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
         amax_out[1] = 1.0f;
         amax_out[2] = 1.0f;
     }
+    const uint32_t dmask = kRHT ? rht_sign_mask(rht_seed) : 0u;
     const int lane = threadIdx.x & 31;
     const int64_t bpr = cols / 16;
     const int64_t ipr = (bpr + kRowItemBlocks - 1) / kRowItemBlocks;
@@ -262,9 +310,20 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
             if (ok[h]) blk[h].load(x + r * ldx + (kb0 + 32 * h) * 16);
         }
         uint32_t bm[2];
+        float tv[kRHT ? 2 : 1][16];  // transformed blocks (RHT only)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            bm[h] = ok[h] ? blk[h].absmax_bits() : 0u;
+            if constexpr (kRHT) {
+                bm[h] = 0u;
+                if (ok[h]) {
+                    blk[h].unpack(tv[h]);
+                    rht16(tv[h], dmask);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) bm[h] = max(bm[h], abs_bits(tv[h][k]));
+                }
+            } else {
+                bm[h] = ok[h] ? blk[h].absmax_bits() : 0u;
+            }
             if constexpr (kMX) bm[h] = max(bm[h], __shfl_xor_sync(0xFFFFFFFFu, bm[h], 1));
         }
 #pragma unroll
@@ -274,17 +333,20 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
             const uint64_t i0 = (uint64_t)r * (uint64_t)cols + (uint64_t)kb * 16;
             uint2 c = make_uint2(0u, 0u);
             uint32_t sb;
-            if constexpr (kMX) {
-                float v[16];
+            float v[16];
+            if constexpr (kRHT) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = tv[h][k];
+            } else {
                 blk[h].unpack(v);
+            }
+            if constexpr (kMX) {
                 c = mx_encode16<kSR>(v, bm[h], seed, i0, status, sb);
             } else {
                 BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc);
                 if (!ts.finite) bs.sb = 0u;
                 sb = bs.sb;
                 if (bs.sb != 0u) {
-                    float v[16];
-                    blk[h].unpack(v);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
                     c = encode16<kSR>(v, seed, i0);
@@ -557,6 +619,16 @@ void launch_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t l
     else launch_amax_t<__nv_bfloat16>(x, rows, cols, ldx, partials, grid, s);
 }
 
+void launch_rht_rows_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
+                          uint32_t* partials, int grid, cudaStream_t s) {
+    if (fp32)
+        rht_rows_amax_kernel<float><<<grid, kQuantThreads, 0, s>>>(static_cast<const float*>(x), rows, cols, ldx,
+                                                                   rht_seed, partials);
+    else
+        rht_rows_amax_kernel<__nv_bfloat16><<<grid, kQuantThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                                                                           rows, cols, ldx, rht_seed, partials);
+}
+
 void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
                      uint32_t* partials, int grid, cudaStream_t s) {
     if (fp32)
@@ -569,19 +641,22 @@ void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64
 
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
-                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, int grid,
-                             cudaStream_t s) {
-#define NVFP4_ROW(T, SR, MX)                                                                                    \
-    quantize_rowwise_kernel<T, SR, MX><<<grid, kQuantThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx, \
-                                                                      partials, npartials, codes, ld_codes, so, \
-                                                                      amax_out, status, seed)
-#define NVFP4_ROW_MX(T, SR) \
-    if (mx) NVFP4_ROW(T, SR, true); else NVFP4_ROW(T, SR, false)
+                             float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
+                             uint64_t rht_seed, int grid, cudaStream_t s) {
+#define NVFP4_ROW(T, SR, MX, RHT)                                                                               \
+    quantize_rowwise_kernel<T, SR, MX, RHT><<<grid, kQuantThreads, 0, s>>>(                                    \
+        static_cast<const T*>(x), rows, cols, ldx, partials, npartials, codes, ld_codes, so, amax_out, status, \
+        seed, rht_seed)
+#define NVFP4_ROW_MX(T, SR, RHT) \
+    if (mx) NVFP4_ROW(T, SR, true, RHT); else NVFP4_ROW(T, SR, false, RHT)
+#define NVFP4_ROW_RHT(T, SR) \
+    if (rht) { NVFP4_ROW_MX(T, SR, true); } else { NVFP4_ROW_MX(T, SR, false); }
     if (fp32) {
-        if (sr) { NVFP4_ROW_MX(float, true); } else { NVFP4_ROW_MX(float, false); }
+        if (sr) { NVFP4_ROW_RHT(float, true) } else { NVFP4_ROW_RHT(float, false) }
     } else {
-        if (sr) { NVFP4_ROW_MX(__nv_bfloat16, true); } else { NVFP4_ROW_MX(__nv_bfloat16, false); }
+        if (sr) { NVFP4_ROW_RHT(__nv_bfloat16, true) } else { NVFP4_ROW_RHT(__nv_bfloat16, false) }
     }
+#undef NVFP4_ROW_RHT
 #undef NVFP4_ROW_MX
 #undef NVFP4_ROW
 }
