@@ -274,6 +274,8 @@ def gpu_bench(args):
 
     mx = None if args.no_mx else mx_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
     rht_rows = None if args.no_mx else rht_rows_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
+    bf16_gemm = None if args.no_mx else bf16_gemm_measure(nv, x, w, flush, stream, max(5, args.steps // 10),
+                                                          _peaks())
 
     if rank != 0:
         if world > 1:
@@ -327,6 +329,7 @@ def gpu_bench(args):
         "gpu_launches": args.steps * sum(launches_per_op.values()),
         "mxfp4": mx,
         "rht_fprop_dgrad_quantize": rht_rows,
+        "bf16_fallback_gemm": bf16_gemm,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -488,6 +491,18 @@ def rht_rows_measure(nv, x, w, dy, flush, stream, steps):
     per = _time_ops(nv, ops, flush, stream, steps)
     return {name: {"ms": round(t / steps, 4), "gbs": round(nbytes[name] / (t / steps * 1e-3) / 1e9, 1)}
             for name, t in per.items()}
+
+
+def bf16_gemm_measure(nv, x, w, flush, stream, steps, peaks):
+    """The BF16 fallback GEMM (kind::f16) at the Fprop shape, for the layers
+    the recipe keeps in high precision.  Not part of `value`."""
+    import torch
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    per = _time_ops(nv, [("gemm_bf16_fprop", lambda: nv.nvfp4_gemm_bf16(x, w, out=y))], flush, stream, steps)
+    ms = per["gemm_bf16_fprop"] / steps
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tflops": round(tf, 1), "peak_bf16_tflops": peaks["bf16"],
+            "frac": round(tf / peaks["bf16"], 4), "peak_source": f"{peaks['source']} cuBLAS bf16 burst"}
 
 
 def mx_measure(nv, x, w, dy, flush, stream, steps):

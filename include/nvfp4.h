@@ -241,6 +241,20 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
                         int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm_bf16 -- C[m][n] = sum_k A[m][k] B[n][k] with bf16 A and B and
+ * FP32 accumulation on the tcgen05 tensor cores (kind::f16): the GEMM of the
+ * linear layers the recipe keeps in high precision (paper page, recipe
+ * paragraph: a few sensitive layers and the final ones stay in BF16).
+ *   A            device bf16 [M][lda], B device bf16 [N][ldb] (both K-major,
+ *                lda, ldb >= K and multiples of 8), K % 8 == 0.
+ *   C            device, [M][ldc] of out_dtype, written whole.
+ *   All pointers 16-byte aligned.  Errors as nvfp4_gemm.
+ */
+nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                             nvfp4_out_dtype out_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             nvfp4_stream_t stream);
+
+/*
  * Linear layer Y = X W^T with NVFP4 GEMMs, following the recipe (paper
  * page: 2D weight scaling keeps Fprop and Dgrad consistent, Hadamard only on
  * Wgrad; blog: stochastic rounding on gradients):

@@ -338,6 +338,20 @@ def dequantize(q: dict) -> np.ndarray:
     return out
 
 
+def bf16_gemm(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """C[m, n] = sum_k a[m, k] * b[n, k] in float64 for bf16-valued inputs
+    (given as float32 arrays holding bf16 values exactly): the high-precision
+    GEMM the recipe keeps for a few layers, as one float64 matmul."""
+    a = np.asarray(a, dtype=np.float32)
+    b = np.asarray(b, dtype=np.float32)
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("K mismatch")
+    bits = np.concatenate([a.view(np.uint32).ravel(), b.view(np.uint32).ravel()])
+    if np.any(bits & 0xFFFF):
+        raise ValueError("inputs must hold bf16 values")
+    return a.astype(np.float64) @ b.astype(np.float64).T
+
+
 def gemm(qa: dict, qb: dict) -> np.ndarray:
     """C[m, n] = sum_k A^[m, k] * B^[n, k] in float64: the FP64 dot of the
     dequantized operands (both quantized along K)."""

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
-    "nvfp4_quantize_noalloc", "nvfp4_rht_quantize_rowwise", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_quantize_noalloc", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
 
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
                                                      vp]
             L.nvfp4_gemm.restype = st
             L.nvfp4_gemm.argtypes = [tp, tp, vp, st, i64, vp, ctypes.c_size_t, vp]
+            L.nvfp4_gemm_bf16.restype = st
+            L.nvfp4_gemm_bf16.argtypes = [vp, i64, vp, i64, vp, st, i64, i64, i64, i64, vp]
             L.nvfp4_linear_fwd.restype = st
             L.nvfp4_linear_fwd.argtypes = [vp, vp, vp, ctypes.POINTER(nvfp4_linear_ctx), vp]
             L.nvfp4_linear_bwd.restype = st
@@ -274,6 +276,23 @@ def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tens
     st = lib().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), out.data_ptr(), od, out.stride(0), None, 0,
                           _stream(stream))
     _check(st, "nvfp4_gemm")
+    return out
+
+
+def nvfp4_gemm_bf16(a: torch.Tensor, b: torch.Tensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """C[M][N] = a @ b^T for bf16 a [M][K], b [N][K] on the tensor cores (FP32 accumulation)."""
+    for t in (a, b):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("a and b must be 2D row-major bf16 CUDA tensors")
+    if a.shape[1] != b.shape[1]:
+        raise ValueError(f"K mismatch: {tuple(a.shape)} vs {tuple(b.shape)}")
+    if out is None:
+        out = torch.empty(a.shape[0], b.shape[0], dtype=out_dtype, device=a.device)
+    od = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32}[out.dtype]
+    st = lib().nvfp4_gemm_bf16(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), out.data_ptr(), od,
+                               out.stride(0), a.shape[0], b.shape[0], a.shape[1], _stream(stream))
+    _check(st, "nvfp4_gemm_bf16")
     return out
 
 

@@ -366,6 +366,44 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     return check_launch("gemm");
 }
 
+nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                             nvfp4_out_dtype out_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    if (!A || !B || !C) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(NVFP4_ERR_INVALID_ARG, "empty GEMM");
+    if (K % 8) return fail(NVFP4_ERR_INVALID_ARG, "K %lld not a multiple of 8", (long long)K);
+    if (lda < K || ldb < K || lda % 8 || ldb % 8)
+        return fail(NVFP4_ERR_INVALID_ARG, "lda, ldb must be >= K and multiples of 8 elements");
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+        return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
+    const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldc < N || (ldc * esz) % 16) return fail(NVFP4_ERR_INVALID_ARG, "ldc must be >= N with 16-byte rows");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+        return fail(NVFP4_ERR_INVALID_ARG, "A, B, C must be 16-byte aligned");
+    DeviceInfo* dev;
+    nvfp4_status st;
+    if ((st = device_info(&dev))) return st;
+    GemmBf16Args g;
+    g.a = A;
+    g.b = B;
+    g.c = C;
+    g.lda = lda;
+    g.ldb = ldb;
+    g.ldc = ldc;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.out_fp32 = out_dtype == NVFP4_OUT_FP32;
+    g.status = dev->status;
+    g.num_sms = dev->num_sms;
+    const char* msg = nullptr;
+    int e = launch_gemm_bf16(g, reinterpret_cast<cudaStream_t>(stream), &msg);
+    if (e == -1) return fail(NVFP4_ERR_UNSUPPORTED, "gemm_bf16: %s", msg ? msg : "unsupported");
+    if (e) return fail(NVFP4_ERR_CUDA, "gemm_bf16: %s", msg ? msg : cudaGetErrorString((cudaError_t)e));
+    return check_launch("gemm_bf16");
+}
+
 static nvfp4_status check_linear_tensor(const nvfp4_tensor* t, int64_t rows, int64_t cols, const char* name) {
     nvfp4_status st = check_out(t, rows, cols, name);
     if (st) return st;

@@ -187,6 +187,25 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// BF16 operands (the high-precision fallback GEMM): kind::f16, K = 16 per
+// instruction, FP32 accumulation.  Instruction descriptor: D = F32 (bits
+// 4-5 = 1), A = B = BF16 (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at
+// bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t instr_desc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // MXFP4: two UE8M0 scales per row per K = 64 (32-element blocks).
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
@@ -264,6 +283,7 @@ struct Params {
     int b_groups;             // 128-row groups of B: ceil(N / 128)
     int out_fp32;
     int mx;                   // MXFP4 operands (UE8M0 scales, 32-element blocks)
+    int bf16;                 // BF16 operands: no scales, 64 K elements per stage, alpha = 1
     uint32_t* status;
 };
 
@@ -293,8 +313,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
             const uint32_t ph = (it / kStages) & 1u;
             if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
             mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
-            tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kt * BKB, mb * BM);
-            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kt * BKB, nb * BN);
+            // a stage is 128 bytes of every row: 256 FP4 codes or 64 bf16 values
+            const int kx = kt * (p.bf16 ? 64 : BKB);
+            tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kx, mb * BM);
+            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kx, nb * BN);
         }
     }
 }
@@ -323,10 +345,16 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
     }
 }
 
-__device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
+// Operand kinds of the MMA loop.  The loop is instantiated once per kind: a
+// run-time choice between the MMA forms inside the loop slowed the issue of
+// every MMA (0.40 -> 0.63 ms at 8192x20480x5120).
+enum MmaKind { kNvf4 = 0, kMxf4 = 1, kBf16 = 2 };
+
+template <int kKind>
+__device__ __forceinline__ void mma_loop(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
                                          uint32_t tmem_base) {
     const Sched S(p);
-    const uint32_t idesc = instr_desc_nvf4(BM, BN, p.mx != 0);
+    const uint32_t idesc = kKind == kBf16 ? instr_desc_bf16(BM, BN) : instr_desc_nvf4(BM, BN, kKind == kMxf4);
     const uint32_t sf_base = tmem_base + kAccCols;
     uint32_t it = 0, tc = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
@@ -335,7 +363,9 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1u;
-            if (!mbar_wait(&ss->full[s], ph, ss, p.status) || !mbar_wait(&ss->sf_full[s], ph, ss, p.status)) return;
+            if (!mbar_wait(&ss->full[s], ph, ss, p.status) ||
+                (kKind != kBf16 && !mbar_wait(&ss->sf_full[s], ph, ss, p.status)))
+                return;
             tc_fence_after();
             const uint32_t sfa_t = sf_base + s * kSfColsPerStage;
             const uint32_t sfb_t = sfa_t + kSfaCols;
@@ -345,15 +375,25 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
             for (int j = 0; j < kMmaPerStage; ++j) {
                 const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
                 const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
-                if (p.mx)
-                    mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+                if constexpr (kKind == kBf16)
+                    mma_bf16(tmem_base, adesc, bdesc, idesc, acc);
+                else if constexpr (kKind == kMxf4)
+                    mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
                 else
-                    mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                    mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
             }
             mma_commit(&ss->empty[s]);
         }
         mma_commit(&ss->acc_full);
     }
+}
+
+__device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
+                                         uint32_t tmem_base) {
+    if (p.bf16) mma_loop<kBf16>(p, ss, sA, sB, tmem_base);
+    else if (p.mx) mma_loop<kMxf4>(p, ss, sA, sB, tmem_base);
+    else mma_loop<kNvf4>(p, ss, sA, sB, tmem_base);
 }
 
 // Scale-factor TMEM layout read by one MMA (measured on the hardware):
@@ -440,7 +480,7 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
                                               uint8_t* stage, uint32_t tmem_base, int q, int h, int lane) {
     const Sched S(p);
-    const float alpha = __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
+    const float alpha = p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
     uint8_t* row_base = stage + lane * 32;
     const int sw = (lane >> 2) & 1;
@@ -555,11 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, sA, sB);
         } else if (warp == 2) {
-            if (lane == 0) scale_producer_role(p, ss, sSf);
+            if (lane == 0 && !p.bf16) scale_producer_role(p, ss, sSf);
         } else if (warp == 1) {
             if (lane == 0) mma_role(p, ss, sA, sB, tmem_base);
         } else if (warp >= 4) {
-            scale_role(p, ss, sSf, tmem_base, warp & 3, lane);
+            if (!p.bf16) scale_role(p, ss, sSf, tmem_base, warp & 3, lane);
         }
     } else {
         const int e = warp - 8;
@@ -668,8 +708,58 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
     p.mx = g.mx;
+    p.bf16 = 0;
     p.status = g.status;
     // persistent: one CTA per SM, at most one per tile
+    const int64_t tiles = (int64_t)p.num_m * p.num_n;
+    const int grid = (int)(tiles < g.num_sms ? tiles : g.num_sms);
+    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tcm, p);
+    return (int)cudaGetLastError();
+}
+
+int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
+    using namespace gemm;
+    if (get_encoder(msg)) return 1;
+    if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) {
+        *msg = "dimension exceeds 2^31";
+        return -1;
+    }
+    CUtensorMap ta, tb, tcm;
+    if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, g.M, g.K, g.lda * 2, 64, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B, msg) ||
+        make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.b, g.N, g.K, g.ldb * 2, 64, BN,
+                 CU_TENSOR_MAP_SWIZZLE_128B, msg))
+        return 1;
+    if (g.out_fp32) {
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.c, g.M, g.N, g.ldc * 4, 8, 32,
+                     CU_TENSOR_MAP_SWIZZLE_32B, msg))
+            return 1;
+    } else {
+        if (make_map(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 16, 32,
+                     CU_TENSOR_MAP_SWIZZLE_32B, msg))
+            return 1;
+    }
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(nvf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return (int)e;
+            g_attr_set[dev] = true;
+        }
+    }
+    Params p = {};
+    p.M = (int)g.M;
+    p.N = (int)g.N;
+    p.K = (int)g.K;
+    p.num_m = (int)((g.M + BM - 1) / BM);
+    p.num_n = (int)((g.N + BN - 1) / BN);
+    p.num_k = (int)((g.K + 63) / 64);
+    p.out_fp32 = g.out_fp32;
+    p.bf16 = 1;
+    p.status = g.status;
     const int64_t tiles = (int64_t)p.num_m * p.num_n;
     const int grid = (int)(tiles < g.num_sms ? tiles : g.num_sms);
     nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tcm, p);

@@ -59,4 +59,17 @@ struct GemmArgs {
 // Returns a cudaError_t-like code (0 ok) and fills `msg` on failure.
 int launch_gemm(const GemmArgs& args, cudaStream_t s, const char** msg);
 
+// BF16 GEMM C = A B^T (gemm.cu, the same kernel with kind::f16 MMAs).
+struct GemmBf16Args {
+    const void* a;  // [M][lda] bf16
+    const void* b;  // [N][ldb] bf16
+    void* c;        // [M][ldc] bf16 or fp32
+    int64_t lda, ldb, ldc;  // elements
+    int64_t M, N, K;
+    int out_fp32;
+    uint32_t* status;
+    int num_sms;
+};
+int launch_gemm_bf16(const GemmBf16Args& args, cudaStream_t s, const char** msg);
+
 }  // namespace nvfp4

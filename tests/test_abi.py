@@ -97,6 +97,16 @@ def test_host_argument_checks_need_no_gpu(L):
     assert L.nvfp4_rht_quantize(16, 0, 24, 32, 32, 0, 0, 0, ctypes.byref(tc2), 16, 8192, None) == q.ERR_INVALID_ARG
 
 
+def test_bf16_gemm_argument_checks_need_no_gpu(L):
+    import quantize_block_scaled_amax_gb300 as q
+    # K % 8 != 0
+    assert L.nvfp4_gemm_bf16(16, 12, 16, 12, 16, 0, 64, 64, 64, 12, None) == q.ERR_INVALID_ARG
+    # misaligned A
+    assert L.nvfp4_gemm_bf16(24, 64, 16, 64, 16, 0, 64, 64, 64, 64, None) == q.ERR_INVALID_ARG
+    # lda < K
+    assert L.nvfp4_gemm_bf16(16, 32, 16, 64, 16, 0, 64, 64, 64, 64, None) == q.ERR_INVALID_ARG
+
+
 def test_gemm_argument_checks_need_no_gpu(L):
     import quantize_block_scaled_amax_gb300 as q
     a = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 1, 0)

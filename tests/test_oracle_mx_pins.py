@@ -116,3 +116,16 @@ def test_mx_gemm_against_exact_brute_force():
 def test_mx_needs_blocks_of_32():
     with pytest.raises(oracle.OracleError):
         oracle.quantize(np.zeros((2, 48), dtype=np.float32), block="mx1x32")
+
+
+def test_bf16_gemm_against_exact_brute_force():
+    import torch
+    g = torch.Generator().manual_seed(2)
+    a = (torch.randn(4, 48, generator=g) * 3).bfloat16().float().numpy()
+    b = torch.randn(3, 48, generator=g).bfloat16().float().numpy()
+    c = oracle.bf16_gemm(a, b)
+    for i in range(4):
+        for j in range(3):
+            assert Fraction(c[i, j]) == sum(Fraction(float(a[i, k])) * Fraction(float(b[j, k])) for k in range(48))
+    with pytest.raises(ValueError):
+        oracle.bf16_gemm(np.full((1, 16), 1.0 + 2.0 ** -20, np.float32), np.ones((1, 16), np.float32))
