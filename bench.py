@@ -231,7 +231,12 @@ def gpu_bench(args):
     ms_per_step = total_ms / args.steps
     value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
 
-    # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd/bwd
+    # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd/bwd.
+    # Every step copies its inputs X, W, dY from pinned host memory and its
+    # results Y, dX, dW back.  The copies run on their own streams (one per
+    # direction) and device buffers are double-buffered, so step i's results
+    # go back while step i+1 computes, as a training loop's data movement
+    # would; the compute itself stays on one stream.
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
@@ -240,34 +245,59 @@ def gpu_bench(args):
         yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
         dxh = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
         dwh = torch.empty(N, K, dtype=torch.float32).pin_memory()
-        xd, wd, dyd = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+        din = [(torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)) for _ in range(2)]
+        dout = [(torch.empty_like(y), torch.empty_like(dx), torch.empty_like(dw)) for _ in range(2)]
+        h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("xw", "dy", "y", "bwd", "in_free", "out_free")}
 
-        def e2e_step():
-            xd.copy_(xh, non_blocking=True)
-            wd.copy_(wh, non_blocking=True)
-            dyd.copy_(dyh, non_blocking=True)
-            nv.nvfp4_linear_fwd(xd, wd, ctx, Y=y)
-            nv.nvfp4_linear_bwd(dyd, xd, ctx, sr_seed=sr, rht_seed=rh, dX=dx, dW=dw)
-            yh.copy_(y, non_blocking=True)
-            dxh.copy_(dx, non_blocking=True)
-            dwh.copy_(dw, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            xd, wd, dyd = din[b]
+            yd, dxd, dwd = dout[b]
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(ev["in_free"][b])
+                xd.copy_(xh, non_blocking=True)
+                wd.copy_(wh, non_blocking=True)
+                ev["xw"][b].record(h2d)
+                dyd.copy_(dyh, non_blocking=True)
+                ev["dy"][b].record(h2d)
+            stream.wait_event(ev["xw"][b])
+            if i >= 2:
+                stream.wait_event(ev["out_free"][b])
+            nv.nvfp4_linear_fwd(xd, wd, ctx, Y=yd)
+            ev["y"][b].record(stream)
+            stream.wait_event(ev["dy"][b])
+            nv.nvfp4_linear_bwd(dyd, xd, ctx, sr_seed=sr, rht_seed=rh, dX=dxd, dW=dwd)
+            ev["bwd"][b].record(stream)
+            ev["in_free"][b].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev["y"][b])
+                yh.copy_(yd, non_blocking=True)
+                d2h.wait_event(ev["bwd"][b])
+                dxh.copy_(dxd, non_blocking=True)
+                dwh.copy_(dwd, non_blocking=True)
+                ev["out_free"][b].record(d2h)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
-        e_steps = max(3, args.steps // 4)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_steps = max(4, args.steps // 4)
+        a, b_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(e_steps):
-            e2e_step()
-        b.record(stream)
+        h2d.wait_event(a)
+        for i in range(e_steps):
+            e2e_step(i)
+        stream.wait_event(ev["out_free"][(e_steps - 1) % 2])
+        b_end.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b_end) / e_steps, dev)
         e2e = {"value": round(world * 3 * gemm_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2 + dyh.numel() * 2),
                "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2 + dwh.numel() * 4),
-               "api": "nvfp4_linear_fwd + nvfp4_linear_bwd, pinned host buffers"}
+               "api": "nvfp4_linear_fwd + nvfp4_linear_bwd with pinned host buffers; copies on one stream per "
+                      "direction, device buffers double-buffered so copies overlap the neighbouring steps' compute"}
     st = nv.nvfp4_sync_status()
     if st != nv.OK:
         raise RuntimeError(f"device status {st} after the timed region")

@@ -269,9 +269,9 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     if ((st = zero_scale_padding(out_colwise, s))) return st;
     int ag = 0;
     if (!mx) {
-        const int64_t units = (rows / 16) * (cols / (fp32 ? 4 : 8));
+        const int64_t units = (rows / 16) * (cols / (fp32 ? 2 : 4));  // 16 rows x one 8-byte vector
         ag = (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads),
-                                                           (int64_t)dev->num_sms * 4, (int64_t)kMaxPartials}));
+                                                           (int64_t)dev->num_sms * 6, (int64_t)kMaxPartials}));
         launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
         if ((st = check_launch("rht_amax"))) return st;
     }

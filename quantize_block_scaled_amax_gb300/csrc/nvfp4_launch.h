@@ -8,7 +8,7 @@ namespace nvfp4 {
 
 constexpr int kAmaxThreads = 256;
 constexpr int kAmaxUnroll = 8;      // 16-byte loads in flight per amax thread
-constexpr int kRhtAmaxThreads = 512;
+constexpr int kRhtAmaxThreads = 256;
 constexpr int kRowItemBlocks = 64;  // 1x16 blocks per warp item of the rowwise quantizer
 constexpr int kQuantThreads = 256;
 constexpr int kColThreads = 128;

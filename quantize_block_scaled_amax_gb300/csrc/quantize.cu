@@ -125,35 +125,98 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const T* __restrict_
 }
 
 // Pass 1 of the RHT path: amax of the transformed tensor.  One unit is 16
-// consecutive rows x one 16-byte column vector (8 bf16 or 4 fp32 columns);
-// every column of the unit is one 16-point chunk.
+// consecutive rows x one 8-byte column vector (4 bf16 or 2 fp32 columns);
+// every column of the unit is one 16-point chunk.  The butterfly runs on
+// column pairs with packed FP32x2 adds (each lane of add.rn.f32x2 is one
+// correctly rounded FP32 add, so the values are those of rht16); the signs
+// d_j are applied to the inputs, and the final exact x1/4 is applied to the
+// maximum (scaling by 1/4 is monotone, so the max of the scaled values is the
+// scaled max).
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+
+// 16-point butterfly of two columns at once (x[j] holds row j of both),
+// without the signs (applied by the caller) and without the final x1/4.
+__device__ __forceinline__ void rht16_pair_unscaled(uint64_t x[16]) {
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int h = 1 << st;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j & h) continue;
+            const uint64_t a = x[j], b = x[j + h];
+            x[j] = f32x2_add(a, b);
+            x[j + h] = f32x2_sub(a, b);
+        }
+    }
+}
+
+// one column pair of the unit: FP32 values of rows 0..15 (signs applied)
 template <typename T>
-__global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
-                                                                int64_t ldx, uint64_t rht_seed,
-                                                                uint32_t* __restrict__ partials) {
+__device__ __forceinline__ void unit_pair(const uint2 raw[16], int pr, uint32_t dmask, uint64_t x[16]);
+
+template <>
+__device__ __forceinline__ void unit_pair<__nv_bfloat16>(const uint2 raw[16], int pr, uint32_t dmask,
+                                                         uint64_t x[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t w = pr ? raw[i].y : raw[i].x;  // two bf16: columns 2pr, 2pr+1
+        if ((dmask >> i) & 1u) w ^= 0x80008000u;
+        x[i] = f32x2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+}
+
+template <>
+__device__ __forceinline__ void unit_pair<float>(const uint2 raw[16], int pr, uint32_t dmask, uint64_t x[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t s = ((dmask >> i) & 1u) << 31;
+        x[i] = f32x2_pack(__uint_as_float(raw[i].x ^ s), __uint_as_float(raw[i].y ^ s));
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* __restrict__ x, int64_t rows,
+                                                                     int64_t cols, int64_t ldx, uint64_t rht_seed,
+                                                                     uint32_t* __restrict__ partials) {
     __shared__ uint32_t red[33];
-    constexpr int V = 16 / sizeof(T);
+    constexpr int V = 8 / sizeof(T);        // columns per 8-byte vector
+    constexpr int kPairs = V / 2;           // column pairs per vector (bf16: 2, fp32: 1)
     const uint32_t dmask = rht_sign_mask(rht_seed);
     const int64_t vpr = cols / V;  // column vectors per row block
     const int64_t nunits = (rows / 16) * vpr;
-    uint32_t m = 0;
+    uint32_t m = 0;  // max |y| bit pattern (a NaN or an infinity gives >= 0x7f800000)
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nunits;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t rb = u / vpr, cv = u - rb * vpr;
         const T* src = x + rb * 16 * ldx + cv * V;
-        uint4 raw[16];
+        uint2 raw[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src + i * ldx));
+        for (int i = 0; i < 16; ++i) raw[i] = __ldg(reinterpret_cast<const uint2*>(src + i * ldx));
 #pragma unroll
-        for (int c = 0; c < V; ++c) {
-            float chunk[16];
+        for (int pr = 0; pr < kPairs; ++pr) {
+            uint64_t v[16];
+            unit_pair<T>(raw, pr, dmask, v);
+            rht16_pair_unscaled(v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) chunk[i] = vec_elem<T>(raw[i], c);
-            rht16(chunk, dmask);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = max(m, abs_bits(chunk[i]));
+            for (int i = 0; i < 16; ++i)
+                m = max(m, max((uint32_t)v[i] & 0x7FFFFFFFu, (uint32_t)(v[i] >> 32) & 0x7FFFFFFFu));
         }
     }
+    // the maximum of fl(|y| / 4) is fl(max |y| / 4) (monotone); a NaN or an
+    // infinity stays a pattern >= 0x7f800000
+    m = __float_as_uint(__fmul_rn(__uint_as_float(m), 0.25f)) & 0x7FFFFFFFu;
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
