@@ -220,7 +220,7 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
     }
 
     if (block == NVFP4_BLOCK_16x16) {
-        const int g = cap_grid(tiles_2d(rows, cols), 8, dev->num_sms);
+        const int g = quantize_2d_grid(rows, cols, fp32, dev->num_sms);
         ScaleOut sr_ = out_rowwise ? scale_out(*out_rowwise) : ScaleOut{};
         ScaleOut sc_ = out_colwise ? scale_out(*out_colwise) : ScaleOut{};
         launch_quantize_2d(x, fp32, rows, cols, ldx, partials, ag, out_rowwise ? out_rowwise->codes : nullptr,

@@ -237,6 +237,8 @@ struct ScaleOut {
     __device__ __forceinline__ int64_t offset(int64_t r, int64_t kb) const {
         return mma ? mma_scale_offset(r, kb, n_katoms) : r * nkb + kb;
     }
+    // offset(r + k, kb) = offset(r, kb) + k * row_step() when r % 4 == 0 and k < 4
+    __device__ __forceinline__ int64_t row_step() const { return mma ? 16 : nkb; }
 };
 
 // ---------------------------------------------------------------------------

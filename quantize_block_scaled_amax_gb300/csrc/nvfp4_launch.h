@@ -35,7 +35,7 @@ void launch_quantize_2d(const void* x, bool fp32, int64_t rows, int64_t cols, in
                         int npartials, uint8_t* codes_r, int64_t ld_r, ScaleOut so_r, float* amax_r, uint8_t* codes_c,
                         int64_t ld_c, ScaleOut so_c, float* amax_c, uint32_t* status, int grid, cudaStream_t s);
 int64_t colwise_tiles(int64_t rows, int64_t cols);
-int64_t tiles_2d(int64_t rows, int64_t cols);
+int quantize_2d_grid(int64_t rows, int64_t cols, bool fp32, int num_sms);
 
 // GEMM (gemm.cu).  A: [M][K] codes/scales (MMA layout), B: [N][K].
 struct GemmArgs {

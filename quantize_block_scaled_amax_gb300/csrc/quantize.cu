@@ -549,24 +549,115 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
 
 // ---------------------------------------------------------------------------
 // Pass 2, 16x16 blocks (weights, RTN): one E4M3 scale per 16x16 tile, codes
-// for x (rowwise) and for x^T (colwise) from one read.  Under RTN the code of
-// an element depends only on the element and its tile's scale, so the codes
-// of x^T are the transpose of those of x.  A CTA covers 64 rows x 128
-// columns (4 x 8 tiles); thread t takes row t/4 and columns 32*(t%4)..+31.
-constexpr int k2dRows = 64;
-constexpr int k2dCols = 128;
+// for x (rowwise) and for x^T (colwise) from one read.  A warp takes a unit
+// of 128 columns by one or two tiles of 16 rows; lane l holds columns
+// 4l..4l+3 of every row of the unit, so a tile's 16 columns sit in four
+// neighbouring lanes and its maximum is two shuffles.  Under RTN a code
+// depends only on the element and its tile's scale, so neighbouring values
+// are converted in pairs twice: along the row for the codes of x, and down
+// the column (rows 2i, 2i+1) for the codes of x^T, which each lane then
+// holds whole for its four columns.  No shared memory is used after the
+// tensor-scale reduction and warps never wait on one another.
+
+// four consecutive elements of one row
+template <typename T>
+struct Quad;
+
+template <>
+struct Quad<__nv_bfloat16> {
+    uint2 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint2*>(p)); }
+    // running maximum of the magnitudes, as packed 16-bit bf16 patterns
+    __device__ __forceinline__ uint32_t absmax_acc(uint32_t acc) const {
+        return __vmaxu2(__vmaxu2(acc, u.x & 0x7FFF7FFFu), u.y & 0x7FFF7FFFu);
+    }
+    __device__ __forceinline__ static uint32_t widen(uint32_t acc) { return max(acc & 0xFFFFu, acc >> 16) << 16; }
+    __device__ __forceinline__ void pairs(uint64_t& p01, uint64_t& p23) const {
+        p01 = f32x2_pack(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u));
+        p23 = f32x2_pack(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    }
+};
+
+template <>
+struct Quad<float> {
+    uint4 u;
+    __device__ __forceinline__ void load(const float* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ uint32_t absmax_acc(uint32_t acc) const { return max(acc, vec_absmax_bits<float>(u)); }
+    __device__ __forceinline__ static uint32_t widen(uint32_t acc) { return acc; }
+    __device__ __forceinline__ void pairs(uint64_t& p01, uint64_t& p23) const {
+        p01 = (uint64_t)u.x | ((uint64_t)u.y << 32);
+        p23 = (uint64_t)u.z | ((uint64_t)u.w << 32);
+    }
+};
+
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float f32x2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
+
+// E2M1 codes (RTN) of v0..v3 in the low 16 bits, v0 in the lowest nibble
+__device__ __forceinline__ uint32_t e2m1x4_rtn(float v0, float v1, float v2, float v3) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 t0, t1;\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "mov.b16 h, {t0, t1};\n\t"
+        "cvt.u32.u16 %0, h;\n\t}"
+        : "=r"(out)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return out;
+}
+
+// E2M1 codes (RTN) of four pairs: byte k holds lo[k] in its low nibble and
+// hi[k] in its high nibble
+__device__ __forceinline__ uint32_t e2m1_pairs4_rtn(const float lo[4], const float hi[4]) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(out)
+        : "f"(lo[0]), "f"(hi[0]), "f"(lo[1]), "f"(hi[1]), "f"(lo[2]), "f"(hi[2]), "f"(lo[3]), "f"(hi[3]));
+    return out;
+}
+
+// 4x4 byte transpose: byte k of out[j] = byte j of w[k]
+__device__ __forceinline__ void byte_transpose4(const uint32_t w[4], uint32_t out[4]) {
+    const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140), t1 = __byte_perm(w[0], w[1], 0x7362);
+    const uint32_t t2 = __byte_perm(w[2], w[3], 0x5140), t3 = __byte_perm(w[2], w[3], 0x7362);
+    out[0] = __byte_perm(t0, t2, 0x5410);
+    out[1] = __byte_perm(t0, t2, 0x7632);
+    out[2] = __byte_perm(t1, t3, 0x5410);
+    out[3] = __byte_perm(t1, t3, 0x7632);
+}
 
 template <typename T>
-__global__ void __launch_bounds__(k2dThreads) quantize_2d_kernel(
+struct Unit2d {
+    static constexpr int kTiles = sizeof(T) == 2 ? 2 : 1;  // 16-row tiles per unit (register budget)
+    static constexpr int kRows = 16 * kTiles;
+    static constexpr int kCols = 128;
+};
+
+template <int N>
+struct TileIdx {
+    static constexpr int value = N;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes_r, int64_t ld_r, ScaleOut so_r, float* amax_r,
     uint8_t* __restrict__ codes_c, int64_t ld_c, ScaleOut so_c, float* amax_c, uint32_t* status) {
+    using U = Unit2d<T>;
+    // bf16: two 16-row register buffers, the loads of the next tile in flight
+    // while one tile is encoded; fp32 quads are twice as wide, so one buffer
+    constexpr bool kPipe = U::kTiles == 2;
     __shared__ uint32_t red[33];
-    __shared__ float bam[k2dRows][k2dCols / 16];
-    __shared__ float tile_r[k2dRows / 16][k2dCols / 16];
-    __shared__ uint32_t tile_sb[k2dRows / 16][k2dCols / 16];
-    __shared__ __align__(16) uint8_t ctile[k2dRows][k2dCols / 2];
-
     float* amax_out = amax_r ? amax_r : amax_c;
     const TensorScales ts = reduce_partials(partials, npartials, amax_out, status, red);
     if (amax_r && amax_c && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -574,96 +665,134 @@ __global__ void __launch_bounds__(k2dThreads) quantize_2d_kernel(
         amax_c[1] = ts.s_dec;
         amax_c[2] = ts.s_enc;
     }
-    const int64_t tiles_r = (rows + k2dRows - 1) / k2dRows;
-    const int64_t tiles_c = (cols + k2dCols - 1) / k2dCols;
-    const int64_t ntiles = tiles_r * tiles_c;
-    const int lr = threadIdx.x / 4, seg = threadIdx.x % 4;
+    const int lane = threadIdx.x & 31;
+    const int qd = lane & 3;  // position of the lane among the four of its tile
+    const int64_t groups = (cols + U::kCols - 1) / U::kCols;
+    const int64_t nunits = ((rows + U::kRows - 1) / U::kRows) * groups;
+    const int64_t nwarps = (int64_t)gridDim.x * (k2dThreads / 32);
+    const int64_t first = (int64_t)blockIdx.x * (k2dThreads / 32) + (threadIdx.x >> 5);
+    const int64_t step_r = so_r.row_step(), step_c = so_c.row_step();
 
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int64_t tile_id = ntiles - 1 - t;
-        const int64_t trow = tile_id / tiles_c;
-        const int64_t r0 = trow * k2dRows, c0 = (tile_id - trow * tiles_c) * k2dCols;
-        const int64_t r = r0 + lr;
-        float v[2][16];
-        bool ok[2];
+    // Tile s of this warp's stream is tile s % kTiles of its unit s / kTiles.
+    struct TilePos {
+        int64_t r, col;  // first row of the tile, first column of the lane
+        bool valid;      // the unit exists (warp-uniform)
+        bool has;        // the tile exists: the last unit may have fewer rows (warp-uniform)
+        bool ok;         // the lane's columns exist
+    };
+    auto tile_pos = [&](int64_t s) {
+        TilePos p{0, 0, false, false, false};
+        const int64_t u = first + (s / U::kTiles) * nwarps;
+        if (u >= nunits) return p;
+        const int64_t unit = nunits - 1 - u;  // last unit first: the end of x is what the amax pass left in L2
+        const int64_t ur = unit / groups;
+        p.col = (unit - ur * groups) * U::kCols + 4 * lane;
+        p.r = ur * U::kRows + 16 * (s % U::kTiles);
+        p.valid = true;
+        p.has = p.r < rows;  // rows % 16 == 0
+        p.ok = p.has && p.col < cols;  // cols % 16 == 0
+        return p;
+    };
+    auto load16 = [&](Quad<T>(&q)[16], const TilePos& p) {
+        const T* src = x + p.r * ldx + p.col;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int64_t c = c0 + 32 * seg + 16 * b;
-            ok[b] = (r < rows) && (c < cols);
-            float m = 0.0f;
-            if (ok[b]) {
-                In<T>::load8(x + r * ldx + c, v[b]);
-                In<T>::load8(x + r * ldx + c + 8, v[b] + 8);
+        for (int i = 0; i < 16; ++i) q[i].load(src + i * ldx);
+    };
+
+    uint32_t cw[4][2 * U::kTiles];  // codes of x^T: 8 bytes per column and tile
+    auto process = [&](const Quad<T>(&q)[16], const TilePos& p, auto tile) {
+        constexpr int t = decltype(tile)::value;
+        if (p.has) {
+            uint32_t acc = 0;
+            if (p.ok) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(v[b][k]));
+                for (int i = 0; i < 16; ++i) acc = q[i].absmax_acc(acc);
             }
-            bam[lr][2 * seg + b] = m;
-        }
-        __syncthreads();
-        if (threadIdx.x < (k2dRows / 16) * (k2dCols / 16)) {
-            const int ti = threadIdx.x / (k2dCols / 16), tj = threadIdx.x % (k2dCols / 16);
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = fmaxf(m, bam[16 * ti + i][tj]);
-            BlockScale bs = block_scale(m, ts.s_enc);
+            uint32_t m = Quad<T>::widen(acc);
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            BlockScale bs = block_scale(__uint_as_float(m), ts.s_enc);
             if (!ts.finite) bs.sb = 0u;
-            tile_sb[ti][tj] = bs.sb;
-            tile_r[ti][tj] = bs.r;
-        }
-        __syncthreads();
-        uint2 c[2];
-        uint32_t sb[2];
+            const bool zero = bs.sb == 0u;  // every code of the tile is 0
+            const uint64_t r2 = f32x2_pack(bs.r, bs.r);
+            uint32_t wk[4];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int tj = 2 * seg + b;
-            sb[b] = tile_sb[lr / 16][tj];
-            c[b] = make_uint2(0u, 0u);
-            if (ok[b] && sb[b] != 0u) {
-                const float rm = tile_r[lr / 16][tj];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[b][k] = __fmul_rn(v[b][k], rm);
-                c[b] = encode16<false>(v[b], 0, 0);
-            }
-        }
-        *reinterpret_cast<uint4*>(&ctile[lr][16 * seg]) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
-        if (codes_r) {
-            uint8_t* dst = codes_r + r * ld_r + (c0 + 32 * seg) / 2;
-            if (ok[0] && ok[1]) {
-                *reinterpret_cast<uint4*>(dst) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
-            } else if (ok[0]) {
-                *reinterpret_cast<uint2*>(dst) = c[0];
-            }
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-                if (ok[b]) so_r.p[so_r.offset(r, (c0 + 32 * seg) / 16 + b)] = (uint8_t)sb[b];
-        }
-        __syncthreads();
-        if (codes_c) {
-            // output row oc = c0 + cc of x^T; 32 rows of x per thread -> 16 bytes
-            const int cc = threadIdx.x / 2, hh = threadIdx.x % 2;
-            const int64_t oc = c0 + cc;
-            const int64_t orow0 = r0 + 32 * hh;
-            if (oc < cols && orow0 < rows) {
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t byte = ctile[32 * hh + i][cc / 2];
-                    const uint32_t nib = (cc & 1) ? (byte >> 4) : (byte & 0xFu);
-                    w[i / 8] |= nib << (4 * (i % 8));
+            for (int i = 0; i < 16; i += 2) {
+                uint64_t a01, a23, b01, b23;
+                q[i].pairs(a01, a23);
+                q[i + 1].pairs(b01, b23);
+                a01 = f32x2_mul(a01, r2);
+                a23 = f32x2_mul(a23, r2);
+                b01 = f32x2_mul(b01, r2);
+                b23 = f32x2_mul(b23, r2);
+                const float a[4] = {f32x2_lo(a01), f32x2_hi(a01), f32x2_lo(a23), f32x2_hi(a23)};
+                const float b[4] = {f32x2_lo(b01), f32x2_hi(b01), f32x2_lo(b23), f32x2_hi(b23)};
+                if (codes_r && p.ok) {
+                    const int64_t r = p.r + i;
+                    const uint32_t ca = zero ? 0u : e2m1x4_rtn(a[0], a[1], a[2], a[3]);
+                    const uint32_t cb = zero ? 0u : e2m1x4_rtn(b[0], b[1], b[2], b[3]);
+                    *reinterpret_cast<uint16_t*>(codes_r + r * ld_r + p.col / 2) = (uint16_t)ca;
+                    *reinterpret_cast<uint16_t*>(codes_r + (r + 1) * ld_r + p.col / 2) = (uint16_t)cb;
                 }
-                uint8_t* dst = codes_c + oc * ld_c + orow0 / 2;
-                const bool full = orow0 + 32 <= rows;
-                if (full) {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-                } else {
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                // rows i, i+1 of the four columns: byte j of wk = column j
+                wk[(i / 2) % 4] = e2m1_pairs4_rtn(a, b);
+                if ((i / 2) % 4 == 3) {
+                    uint32_t c4[4];
+                    byte_transpose4(wk, c4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cw[j][2 * t + i / 8] = zero ? 0u : c4[j];
                 }
-                const int tj = cc / 16;
-                so_c.p[so_c.offset(oc, orow0 / 16)] = (uint8_t)tile_sb[2 * hh][tj];
-                if (full) so_c.p[so_c.offset(oc, orow0 / 16 + 1)] = (uint8_t)tile_sb[2 * hh + 1][tj];
+            }
+            if (p.ok) {
+                if (codes_r) {
+                    uint8_t* sp = so_r.p + so_r.offset(p.r + 4 * qd, p.col / 16);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) sp[k * step_r] = (uint8_t)bs.sb;
+                }
+                if (codes_c) {
+                    uint8_t* sp = so_c.p + so_c.offset(p.col, p.r / 16);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sp[j * step_c] = (uint8_t)bs.sb;
+                }
             }
         }
-        __syncthreads();
+        if (t == U::kTiles - 1 && codes_c && p.valid && p.col < cols) {
+            // the unit is done: 8 bytes of x^T per column and tile
+            const int64_t r0 = p.r - 16 * t;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint8_t* dst = codes_c + (p.col + j) * ld_c + r0 / 2;
+                bool stored = false;
+                if constexpr (t == 1) {
+                    if (p.has) {
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(cw[j][0], cw[j][1], cw[j][2], cw[j][3]);
+                        stored = true;
+                    }
+                }
+                if (!stored) *reinterpret_cast<uint2*>(dst) = make_uint2(cw[j][0], cw[j][1]);
+            }
+        }
+    };
+
+    Quad<T> qa[16];
+    TilePos pa = tile_pos(0);
+    if (pa.ok) load16(qa, pa);
+    if constexpr (kPipe) {
+        Quad<T> qb[16];
+        for (int64_t s = 0; pa.valid; s += 2) {
+            const TilePos pb = tile_pos(s + 1);  // tile 1 of this unit
+            if (pb.ok) load16(qb, pb);
+            process(qa, pa, TileIdx<0>{});
+            pa = tile_pos(s + 2);  // tile 0 of the next unit
+            if (pa.ok) load16(qa, pa);
+            process(qb, pb, TileIdx<1>{});
+        }
+    } else {
+        for (int64_t s = 0; pa.valid;) {
+            process(qa, pa, TileIdx<0>{});
+            pa = tile_pos(++s);
+            if (pa.ok) load16(qa, pa);
+        }
     }
 }
 
@@ -764,8 +893,21 @@ int64_t colwise_tiles(int64_t rows, int64_t cols) {
     return ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
 }
 
-int64_t tiles_2d(int64_t rows, int64_t cols) {
-    return ((rows + k2dRows - 1) / k2dRows) * ((cols + k2dCols - 1) / k2dCols);
+int quantize_2d_grid(int64_t rows, int64_t cols, bool fp32, int num_sms) {
+    // the kernel loops over its units, so the grid is what stays resident at once
+    static int occ[2] = {0, 0};
+    int& o = occ[fp32 ? 1 : 0];
+    if (o == 0) {
+        int n = 0;
+        cudaError_t e = fp32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_2d_kernel<float>, k2dThreads, 0)
+                             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_2d_kernel<__nv_bfloat16>,
+                                                                             k2dThreads, 0);
+        o = (e == cudaSuccess && n > 0) ? n : 2;
+    }
+    const int64_t unit_rows = fp32 ? Unit2d<float>::kRows : Unit2d<__nv_bfloat16>::kRows;
+    const int64_t units = ((rows + unit_rows - 1) / unit_rows) * ((cols + 127) / 128);
+    const int64_t ctas = (units + k2dThreads / 32 - 1) / (k2dThreads / 32);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)o * num_sms));
 }
 
 }  // namespace nvfp4

@@ -119,6 +119,25 @@ def test_2d_16x16_both_layouts(nv, shape, dtype, layout):
     np.testing.assert_array_equal(ur, uc.T)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("side", ["rowwise", "colwise"])
+def test_2d_16x16_one_side_of_a_strided_view(nv, dtype, side):
+    # columns 0..335 of a [208][400] tensor: row stride 400 > cols, a last
+    # 32-row unit with one 16-row tile, a partial 128-column group
+    big = workloads.normal_with_outliers(208, 400, std=0.02, seed=77, dtype=dtype)
+    wn = to_f32_np(big[:, :336].contiguous())
+    view = big.cuda()[:, :336]
+    assert view.stride(0) == 400
+    qr, qc = nv.nvfp4_quantize(view, block="16x16", rowwise=side == "rowwise", colwise=side == "colwise")
+    torch.cuda.synchronize()
+    if side == "rowwise":
+        assert qc is None
+        assert_quant_equal(qr, oracle.quantize(wn, block="16x16"), what="2d rowwise only")
+    else:
+        assert qr is None
+        assert_quant_equal(qc, oracle.quantize(wn, layout="col", block="16x16"), what="2d colwise only")
+
+
 @pytest.mark.parametrize("shape", [(16, 16), (64, 48), (256, 320), (400, 272)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("rounding", ["rtn", "sr"])
