@@ -150,31 +150,49 @@ __device__ __forceinline__ float e2m1_sr_value(float v, uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  Round i uses the key
+// (k0 + i * 0x9E3779B9, k1 + i * 0xBB67AE85); PhiloxKey holds the ten round
+// keys of one seed, built once on the host, so a kernel that takes it as a
+// __grid_constant__ parameter reads them from the constant bank instead of
+// recomputing the key schedule in every call.
+struct PhiloxKey {
+    uint32_t k0[10], k1[10];
+};
+
+__host__ __device__ inline PhiloxKey philox_key(uint64_t seed) {
+    PhiloxKey k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        k.k0[i] = a;
+        k.k1[i] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
+    }
+    return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& k) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
         const uint64_t p0 = 0xD2511F53ull * c.x;  // one 32x32 -> 64-bit multiply each
         const uint64_t p1 = 0xCD9E8D57ull * c.z;
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k0[i], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k.k1[i],
+                       (uint32_t)p0);
     }
     return c;
 }
 
 // Random words of elements i0..i0+3 (i0 % 4 == 0) of a logical tensor for
 // stochastic rounding: counter (i0/4 low, i0/4 high, 0, 0), key = seed.
-__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t i0) {
+__device__ __forceinline__ uint4 sr_words(const PhiloxKey& key, uint64_t i0) {
     uint64_t q = i0 >> 2;
-    return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+    return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), key);
 }
 
 // Encode 16 consecutive elements of one block (already multiplied by r) into
 // 8 bytes.  SR: i0 is the logical index of element 0 (multiple of 16).
 template <bool kSR>
-__device__ __forceinline__ uint2 encode16(const float v[16], uint64_t seed, uint64_t i0) {
+__device__ __forceinline__ uint2 encode16(const float v[16], const PhiloxKey& key, uint64_t i0) {
     uint2 out;
     if constexpr (!kSR) {
         out.x = e2m1x8_rtn(v);
@@ -183,7 +201,7 @@ __device__ __forceinline__ uint2 encode16(const float v[16], uint64_t seed, uint
         float y[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 r = sr_words(seed, i0 + 4 * q);
+            const uint4 r = sr_words(key, i0 + 4 * q);
             y[4 * q + 0] = e2m1_sr_value(v[4 * q + 0], r.x);
             y[4 * q + 1] = e2m1_sr_value(v[4 * q + 1], r.y);
             y[4 * q + 2] = e2m1_sr_value(v[4 * q + 2], r.z);
@@ -219,7 +237,7 @@ __device__ __forceinline__ void rht16(float x[16], uint32_t dmask) {
 }
 
 __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t rht_seed) {
-    uint4 w = philox4x32_10(make_uint4(0u, 0u, 1u, 0u), (uint32_t)rht_seed, (uint32_t)(rht_seed >> 32));
+    uint4 w = philox4x32_10(make_uint4(0u, 0u, 1u, 0u), philox_key(rht_seed));
     return w.x & 0xFFFFu;
 }
 

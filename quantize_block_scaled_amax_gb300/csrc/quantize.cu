@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kQuantThreads) rht_rows_amax_kernel(const T* _
 // ---------------------------------------------------------------------------
 // Quantize one block of 16 values in place into 8 bytes of codes.
 template <bool kSR>
-__device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales& ts, uint64_t seed, uint64_t i0,
+__device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales& ts, const PhiloxKey& key, uint64_t i0,
                                                 uint32_t& sb_out) {
     float bamax = 0.0f;
 #pragma unroll
@@ -244,7 +244,7 @@ __device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales&
     if (bs.sb == 0u) return make_uint2(0u, 0u);
 #pragma unroll
     for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
-    return encode16<kSR>(v, seed, i0);
+    return encode16<kSR>(v, key, i0);
 }
 
 // ---------------------------------------------------------------------------
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kQuantThreads) rht_rows_amax_kernel(const T* _
 // holding a NaN or an infinity flags the status word and gets zero codes and
 // scale; an all-zero block gets zero codes and scale 0.
 template <bool kSR>
-__device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, uint64_t seed, uint64_t i0,
+__device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, const PhiloxKey& key, uint64_t i0,
                                              uint32_t* status, uint32_t& sb_out) {
     if (bmax_bits >= 0x7f800000u) {
         atomicOr(status, kStatusNonfinite);
@@ -327,7 +327,7 @@ __device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, ui
     const float mul = mx_multiplier(sb);
 #pragma unroll
     for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], mul);
-    return encode16<kSR>(v, seed, i0);
+    return encode16<kSR>(v, key, i0);
 }
 
 // ---------------------------------------------------------------------------
@@ -345,7 +345,7 @@ template <typename T, bool kSR, bool kMX, bool kRHT>
 __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantize_rowwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
-    uint64_t seed, uint64_t rht_seed) {
+    const __grid_constant__ PhiloxKey key, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
     TensorScales ts{};
     if constexpr (!kMX) {
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
                 blk[h].unpack(v);
             }
             if constexpr (kMX) {
-                c = mx_encode16<kSR>(v, bm[h], seed, i0, status, sb);
+                c = mx_encode16<kSR>(v, bm[h], key, i0, status, sb);
             } else {
                 BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc);
                 if (!ts.finite) bs.sb = 0u;
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
                 if (bs.sb != 0u) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
-                    c = encode16<kSR>(v, seed, i0);
+                    c = encode16<kSR>(v, key, i0);
                 }
             }
             *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
@@ -433,7 +433,7 @@ template <typename T, bool kSR, bool kRHT, bool kMX>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
-    uint64_t seed, uint64_t rht_seed) {
+    const __grid_constant__ PhiloxKey key, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
     __shared__ __align__(16) T tile[kColTileRows][kColTileCols];
     TensorScales ts{};
@@ -501,8 +501,8 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
                         for (int i = 0; i < 16; ++i) bm = max(bm, max(abs_bits(v0[i]), abs_bits(v1[i])));
                         const uint64_t i0 = (uint64_t)oc * (uint64_t)rows + orow0 + 32 * pb;
                         uint32_t sb;
-                        const uint2 c0 = mx_encode16<kSR>(v0, bm, seed, i0, status, sb);
-                        const uint2 c1 = mx_encode16<kSR>(v1, bm, seed, i0 + 16, status, sb);
+                        const uint2 c0 = mx_encode16<kSR>(v0, bm, key, i0, status, sb);
+                        const uint2 c1 = mx_encode16<kSR>(v1, bm, key, i0 + 16, status, sb);
                         w[4 * pb] = c0.x;
                         w[4 * pb + 1] = c0.y;
                         w[4 * pb + 2] = c1.x;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
                         float v[16];
                         load_chunk(b, v);
                         uint32_t sb;
-                        uint2 c = quantize_block<kSR>(v, ts, seed, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
+                        uint2 c = quantize_block<kSR>(v, ts, key, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
                         w[2 * b] = c.x;
                         w[2 * b + 1] = c.y;
                         sbs |= sb << (8 * b);
@@ -835,10 +835,11 @@ void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t col
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
                              float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
                              uint64_t rht_seed, int grid, cudaStream_t s) {
+    const PhiloxKey key = philox_key(seed);
 #define NVFP4_ROW(T, SR, MX, RHT)                                                                               \
     quantize_rowwise_kernel<T, SR, MX, RHT><<<grid, kQuantThreads, 0, s>>>(                                    \
         static_cast<const T*>(x), rows, cols, ldx, partials, npartials, codes, ld_codes, so, amax_out, status, \
-        seed, rht_seed)
+        key, rht_seed)
 #define NVFP4_ROW_MX(T, SR, RHT) \
     if (mx) NVFP4_ROW(T, SR, true, RHT); else NVFP4_ROW(T, SR, false, RHT)
 #define NVFP4_ROW_RHT(T, SR) \
@@ -857,10 +858,11 @@ void launch_quantize_colwise(const void* x, bool fp32, int64_t rows, int64_t col
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
                              float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,
                              uint64_t rht_seed, int grid, cudaStream_t s) {
+    const PhiloxKey key = philox_key(seed);
 #define NVFP4_COL(T, SR, RHT, MX)                                                                                    \
     quantize_colwise_kernel<T, SR, RHT, MX><<<grid, kColThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx,  \
                                                                          partials, npartials, codes, ld_codes, so,   \
-                                                                         amax_out, status, seed, rht_seed)
+                                                                         amax_out, status, key, rht_seed)
 #define NVFP4_COL_MX(T, SR, RHT) \
     if (mx) NVFP4_COL(T, SR, RHT, true); else NVFP4_COL(T, SR, RHT, false)
 #define NVFP4_COL_RHT(T, SR) \
