@@ -173,14 +173,15 @@ def gpu_bench(args):
         ("quant_w_16x16_both", lambda: nv.nvfp4_quantize(w, block="16x16", colwise=True, out_rowwise=ctx.wq,
                                                          out_colwise=ctx.wtq)),
         ("gemm_fprop", lambda: nv.nvfp4_gemm(ctx.xq, ctx.wq, out=y)),
-        ("quant_dy_1x16_sr", lambda: nv.nvfp4_quantize(dy, round="sr", seed=sr, out_rowwise=ctx.dyq)),
+        # dY rowwise (Dgrad) and RHT colwise (Wgrad), SR, both tensor amaxes from one read
+        ("quant_dy_sr_and_rht", lambda: nv.nvfp4_quantize_with_rht(dy, round="sr", seed=sr, rht_seed=rh,
+                                                                     out_rowwise=ctx.dyq, out_colwise=ctx.dytq)),
         ("gemm_dgrad", lambda: nv.nvfp4_gemm(ctx.dyq, ctx.wtq, out=dx)),
-        ("rht_quant_dy_sr", lambda: nv.nvfp4_rht_quantize(dy, round="sr", seed=sr, rht_seed=rh, out_colwise=ctx.dytq)),
         ("rht_quant_x_rtn", lambda: nv.nvfp4_rht_quantize(x, round="rtn", rht_seed=rh, out_colwise=ctx.xtq)),
         ("gemm_wgrad", lambda: nv.nvfp4_gemm(ctx.dytq, ctx.xtq, out=dw)),
     ]
-    launches_per_op = {"quant_x_1x16_rtn": 2, "quant_w_16x16_both": 2, "gemm_fprop": 1, "quant_dy_1x16_sr": 2,
-                       "gemm_dgrad": 1, "rht_quant_dy_sr": 2, "rht_quant_x_rtn": 2, "gemm_wgrad": 1}
+    launches_per_op = {"quant_x_1x16_rtn": 2, "quant_w_16x16_both": 2, "gemm_fprop": 1, "quant_dy_sr_and_rht": 3,
+                       "gemm_dgrad": 1, "rht_quant_x_rtn": 2, "gemm_wgrad": 1}
     # algorithmic bytes: the amax pass reads the input once, the encode pass
     # reads it again and writes codes (1/2 byte per element) and one E4M3
     # scale per 16 elements per layout
@@ -188,8 +189,8 @@ def gpu_bench(args):
     op_bytes = {
         "quant_x_1x16_rtn": 2 * bx + M * K // 2 + M * K // 16,
         "quant_w_16x16_both": 2 * bw + 2 * (N * K // 2 + N * K // 16),
-        "quant_dy_1x16_sr": 2 * bdy + M * N // 2 + M * N // 16,
-        "rht_quant_dy_sr": 2 * bdy + M * N // 2 + M * N // 16,
+        # one amax read, two encode reads, codes and scales of both layouts
+        "quant_dy_sr_and_rht": 3 * bdy + 2 * (M * N // 2 + M * N // 16),
         "rht_quant_x_rtn": 2 * bx + M * K // 2 + M * K // 16,
     }
     gemm_flops = 2.0 * M * N * K

@@ -126,8 +126,11 @@ typedef struct {
  * (0 for invalid arguments). */
 size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout);
 
-/* Workspace bytes needed by the quantize, RHT-quantize and GEMM calls for
- * any shape (the amax pass keeps one partial per CTA there). */
+/* Workspace bytes that every call taking a workspace accepts, for any
+ * shape: the amax pass keeps one partial per CTA there (2048 at most, 8 KB);
+ * nvfp4_quantize_with_rht keeps two sets (16 KB), which is what this
+ * returns.  nvfp4_quantize, nvfp4_rht_quantize and nvfp4_rht_quantize_rowwise
+ * need only the first 8 KB. */
 size_t nvfp4_workspace_size(void);
 
 /*
@@ -205,6 +208,31 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
                                 nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_with_rht -- one operand of a linear layer for both of its
+ * GEMMs (the paper page's recipe: the Fprop/Dgrad operand without the
+ * transform, the Wgrad operand with it along the tokens).  Results are bit
+ * for bit those of the two separate calls
+ *   nvfp4_quantize(x, block 1x16, round, seed, out_rowwise, NULL)
+ *   nvfp4_rht_quantize(x, round, seed, rht_seed, out_colwise)
+ * but the two tensor amaxes (of x and of the transformed x) come from one
+ * read of x instead of two.
+ *   out_rowwise  describes x, [rows][cols], 1x16 blocks along cols.
+ *   out_colwise  describes y^T, [cols][rows], y the 16-point RHT of x along
+ *                its rows (as nvfp4_rht_quantize); rows % 16 == 0.
+ *                Both outputs are required and must have format NVFP4
+ *                (MXFP4 has no amax pass to share: use the separate calls).
+ *   round, seed  used by both outputs (SR: the same Philox key; each output
+ *                indexes the stream by its own logical element index).
+ *   workspace    device, >= 2 * 8 KB (nvfp4_workspace_size()), 16-byte
+ *                aligned; NVFP4_ERR_WORKSPACE if smaller.
+ *   Other arguments as nvfp4_quantize.
+ */
+nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                     nvfp4_round round, uint64_t seed, uint64_t rht_seed,
+                                     const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
+                                     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_rht_quantize_rowwise -- the 16-point RHT along each row (the GEMM's
  * K for a rowwise operand: each 1x16 block is one transform chunk), then the
  * tensor amax of the result and rowwise quantization.  The paper page allows
@@ -260,12 +288,14 @@ nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t 
  * Wgrad; blog: stochastic rounding on gradients):
  *   fwd:  X -> xq (1x16 RTN);  W -> wq and wtq (16x16 RTN, both layouts);
  *         Y[M][N] (bf16) = gemm(xq, wq).
- *   bwd:  dY -> dyq (1x16 SR);  dX[M][K] (bf16) = gemm(dyq, wtq);
- *         RHT along tokens with rht_seed, then dY^T -> dytq (SR) and
- *         X^T -> xtq (RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
+ *   bwd:  dY -> dyq (1x16 SR) and, after the RHT along tokens with
+ *         rht_seed, dY^T -> dytq (SR), both from one amax read
+ *         (nvfp4_quantize_with_rht);  dX[M][K] (bf16) = gemm(dyq, wtq);
+ *         X^T -> xtq (RHT, RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
  * The context holds caller-allocated quantized buffers; every tensor's
  * rows/cols/ld_codes/scale_layout (MMA) must be filled in for the shapes
- * above, and the workspace as for nvfp4_quantize.  X, W, dY are bf16,
+ * above, and the workspace must have nvfp4_workspace_size() bytes (16 KB,
+ * for nvfp4_quantize_with_rht).  X, W, dY are bf16,
  * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
  * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).
  */

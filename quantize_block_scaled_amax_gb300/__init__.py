@@ -20,7 +20,8 @@ from . import build as _build
 
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
-    "nvfp4_quantize_noalloc", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16", "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
+    "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
 
@@ -86,6 +87,9 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_rht_quantize.restype = st
             L.nvfp4_rht_quantize.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t, vp]
             L.nvfp4_rht_quantize_rowwise.restype = st
+            L.nvfp4_quantize_with_rht.restype = st
+            L.nvfp4_quantize_with_rht.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, tp, vp, ctypes.c_size_t,
+                                                  vp]
             L.nvfp4_rht_quantize_rowwise.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t,
                                                      vp]
             L.nvfp4_gemm.restype = st
@@ -247,6 +251,28 @@ def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_s
                                   rht_seed, ctypes.byref(c), ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "nvfp4_rht_quantize")
     return out_colwise
+
+
+def nvfp4_quantize_with_rht(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,
+                            scale_layout: str = "mma", out_rowwise: QTensor | None = None,
+                            out_colwise: QTensor | None = None, stream=None) -> tuple[QTensor, QTensor]:
+    """Both quantizations of one linear-layer operand from one amax read:
+    (1x16 NVFP4 of x, 1x16 NVFP4 of the RHT of x along its rows, transposed).
+    Bit for bit nvfp4_quantize(x) and nvfp4_rht_quantize(x) with the same
+    round and seed."""
+    _check_input(x)
+    rows, cols = x.shape
+    if out_rowwise is None:
+        out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout)
+    if out_colwise is None:
+        out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
+    r, c = out_rowwise.c(), out_colwise.c()
+    ws = _workspace(x.device)
+    st = lib().nvfp4_quantize_with_rht(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
+                                       rht_seed, ctypes.byref(r), ctypes.byref(c), ws.data_ptr(), ws.numel(),
+                                       _stream(stream))
+    _check(st, "nvfp4_quantize_with_rht")
+    return out_rowwise, out_colwise
 
 
 def nvfp4_rht_quantize_rowwise(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_seed: int = 0, *,

@@ -147,6 +147,13 @@ int cap_grid(int64_t units, int per_sm, int num_sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)num_sms * per_sm));
 }
 
+// CTAs of the RHT amax pass: a unit is 16 rows x one 8-byte column vector
+int rht_amax_grid(int64_t rows, int64_t cols, bool fp32, int num_sms) {
+    const int64_t units = (rows / 16) * (cols / (fp32 ? 2 : 4));
+    return (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads),
+                                                       (int64_t)num_sms * 6, (int64_t)kMaxPartials}));
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -158,7 +165,7 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout) {
     return scales_bytes(rows, cols, scale_layout);
 }
 
-size_t nvfp4_workspace_size(void) { return (size_t)kMaxPartials * sizeof(uint32_t); }
+size_t nvfp4_workspace_size(void) { return 2 * (size_t)kMaxPartials * sizeof(uint32_t); }
 
 const char* nvfp4_last_error(void) { return g_err; }
 
@@ -269,9 +276,7 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     if ((st = zero_scale_padding(out_colwise, s))) return st;
     int ag = 0;
     if (!mx) {
-        const int64_t units = (rows / 16) * (cols / (fp32 ? 2 : 4));  // 16 rows x one 8-byte vector
-        ag = (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads),
-                                                           (int64_t)dev->num_sms * 6, (int64_t)kMaxPartials}));
+        ag = rht_amax_grid(rows, cols, fp32, dev->num_sms);
         launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
         if ((st = check_launch("rht_amax"))) return st;
     }
@@ -279,6 +284,49 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
     launch_quantize_colwise(x, fp32, rows, cols, ldx, partials, ag, out_colwise->codes, out_colwise->ld_codes,
                             scale_out(*out_colwise), out_colwise->amax, dev->status, round == NVFP4_SR, mx, seed,
                             true, rht_seed, g, s);
+    return check_launch("rht_quantize_colwise");
+}
+
+nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                                     nvfp4_round round, uint64_t seed, uint64_t rht_seed,
+                                     const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
+                                     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    nvfp4_status st = check_input(x, dtype, rows, cols, ldx);
+    if (st) return st;
+    if (round != NVFP4_RTN && round != NVFP4_SR) return fail(NVFP4_ERR_INVALID_ARG, "bad round %d", round);
+    if (!out_rowwise || !out_colwise) return fail(NVFP4_ERR_INVALID_ARG, "both outputs are required");
+    if (rows % 16) return fail(NVFP4_ERR_INVALID_ARG, "RHT needs rows %% 16 == 0");
+    if ((st = check_out(out_rowwise, rows, cols, "out_rowwise")) || (st = check_out(out_colwise, cols, rows, "out_colwise")))
+        return st;
+    if (out_rowwise->format != NVFP4_FORMAT_NVFP4 || out_colwise->format != NVFP4_FORMAT_NVFP4)
+        return fail(NVFP4_ERR_INVALID_ARG, "outputs must have format NVFP4 (MXFP4 has no amax pass to share)");
+    if (!workspace || workspace_bytes < 2 * (size_t)kMaxPartials * sizeof(uint32_t))
+        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", 2 * (size_t)kMaxPartials * 4,
+                    workspace_bytes);
+    if (!aligned16(workspace)) return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    DeviceInfo* dev;
+    if ((st = device_info(&dev))) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool fp32 = dtype == NVFP4_IN_FP32;
+    const bool sr = round == NVFP4_SR;
+    uint32_t* partials_rht = static_cast<uint32_t*>(workspace);
+    uint32_t* partials_plain = partials_rht + kMaxPartials;
+    if ((st = zero_scale_padding(out_rowwise, s)) || (st = zero_scale_padding(out_colwise, s))) return st;
+    // one read of x for both tensor scales: amax of the transform and of x
+    const int ag = rht_amax_grid(rows, cols, fp32, dev->num_sms);
+    launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials_rht, ag, s, partials_plain);
+    if ((st = check_launch("rht_amax"))) return st;
+    const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
+    const int gr = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
+    launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials_plain, ag, out_rowwise->codes, out_rowwise->ld_codes,
+                            scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, false, seed, false, 0, gr, s);
+    if ((st = check_launch("quantize_rowwise"))) return st;
+    const int gc = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
+    launch_quantize_colwise(x, fp32, rows, cols, ldx, partials_rht, ag, out_colwise->codes, out_colwise->ld_codes,
+                            scale_out(*out_colwise), out_colwise->amax, dev->status, sr, false, seed, true, rht_seed,
+                            gc, s);
     return check_launch("rht_quantize_colwise");
 }
 
@@ -442,15 +490,14 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
     if ((st = check_linear_tensor(&ctx->wtq, K, N, "wtq")) || (st = check_linear_tensor(&ctx->dyq, M, N, "dyq")) ||
         (st = check_linear_tensor(&ctx->dytq, N, M, "dytq")) || (st = check_linear_tensor(&ctx->xtq, K, M, "xtq")))
         return st;
-    // Dgrad: dX = dY W with SR gradients and the 16x16 weight codes of W^T
-    if ((st = nvfp4_quantize(dY, NVFP4_IN_BF16, M, N, N, NVFP4_BLOCK_1x16, NVFP4_SR, sr_seed, &ctx->dyq, nullptr,
-                             ctx->workspace, ctx->workspace_bytes, stream)))
+    // dY with SR, for both GEMMs from one amax read: rowwise for Dgrad, and
+    // transformed along the tokens, transposed, for Wgrad
+    if ((st = nvfp4_quantize_with_rht(dY, NVFP4_IN_BF16, M, N, N, NVFP4_SR, sr_seed, rht_seed, &ctx->dyq, &ctx->dytq,
+                                      ctx->workspace, ctx->workspace_bytes, stream)))
         return st;
+    // Dgrad: dX = dY W with the 16x16 weight codes of W^T
     if ((st = nvfp4_gemm(&ctx->dyq, &ctx->wtq, dX, NVFP4_OUT_BF16, K, nullptr, 0, stream))) return st;
     // Wgrad: dW = dY^T X with both operands transformed along the tokens
-    if ((st = nvfp4_rht_quantize(dY, NVFP4_IN_BF16, M, N, N, NVFP4_SR, sr_seed, rht_seed, &ctx->dytq,
-                                 ctx->workspace, ctx->workspace_bytes, stream)))
-        return st;
     if ((st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
                                  ctx->workspace_bytes, stream)))
         return st;
@@ -504,9 +551,9 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t
                                     const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
                                     nvfp4_stream_t stream) {
     g_err[0] = 0;
-    // A call never needs more partial slots than the workspace contract
-    // states; refuse if the fixed array were ever smaller than that.
-    const size_t need = nvfp4_workspace_size();
+    // nvfp4_quantize keeps one partial per amax CTA (kMaxPartials at most);
+    // refuse if the fixed array were ever smaller than that.
+    const size_t need = (size_t)kMaxPartials * sizeof(uint32_t);
     if (need > sizeof(g_noalloc_scratch))
         return fail(NVFP4_ERR_WORKSPACE, "quantize needs %zu bytes of scratch, the fixed array holds %zu", need,
                     sizeof(g_noalloc_scratch));

@@ -19,8 +19,9 @@ struct ScaleOut;
 
 void launch_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint32_t* partials, int grid,
                  cudaStream_t s);
+// partials_plain non-null: the same pass also writes the amax partials of x itself
 void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
-                     uint32_t* partials, int grid, cudaStream_t s);
+                     uint32_t* partials, int grid, cudaStream_t s, uint32_t* partials_plain = nullptr);
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,
                              const uint32_t* partials, int npartials, uint8_t* codes, int64_t ld_codes, ScaleOut so,
                              float* amax_out, uint32_t* status, bool sr, bool mx, uint64_t seed, bool rht,

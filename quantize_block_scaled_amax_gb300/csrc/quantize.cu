@@ -186,10 +186,27 @@ __device__ __forceinline__ void unit_pair<float>(const uint2 raw[16], int pr, ui
     }
 }
 
+// kPlain: the same pass also takes the amax of x itself (partials_plain),
+// so an operand quantized both rowwise and transformed-colwise is read once
+// for its two tensor scales.
 template <typename T>
-__global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* __restrict__ x, int64_t rows,
+__device__ __forceinline__ uint32_t raw_absmax_acc(uint32_t acc, uint2 w);
+
+template <>
+__device__ __forceinline__ uint32_t raw_absmax_acc<__nv_bfloat16>(uint32_t acc, uint2 w) {
+    return __vmaxu2(__vmaxu2(acc, w.x & 0x7FFF7FFFu), w.y & 0x7FFF7FFFu);  // packed bf16 magnitudes
+}
+
+template <>
+__device__ __forceinline__ uint32_t raw_absmax_acc<float>(uint32_t acc, uint2 w) {
+    return max(acc, max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu));
+}
+
+template <typename T, bool kPlain>
+__global__ void __launch_bounds__(kRhtAmaxThreads, kPlain ? 2 : 3) rht_amax_kernel(const T* __restrict__ x, int64_t rows,
                                                                      int64_t cols, int64_t ldx, uint64_t rht_seed,
-                                                                     uint32_t* __restrict__ partials) {
+                                                                     uint32_t* __restrict__ partials,
+                                                                     uint32_t* __restrict__ partials_plain) {
     __shared__ uint32_t red[33];
     constexpr int V = 8 / sizeof(T);        // columns per 8-byte vector
     constexpr int kPairs = V / 2;           // column pairs per vector (bf16: 2, fp32: 1)
@@ -197,6 +214,7 @@ __global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* _
     const int64_t vpr = cols / V;  // column vectors per row block
     const int64_t nunits = (rows / 16) * vpr;
     uint32_t m = 0;  // max |y| bit pattern (a NaN or an infinity gives >= 0x7f800000)
+    uint32_t mp = 0;  // kPlain: max |x| (packed 16-bit patterns for bf16)
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nunits;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t rb = u / vpr, cv = u - rb * vpr;
@@ -204,6 +222,10 @@ __global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* _
         uint2 raw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) raw[i] = __ldg(reinterpret_cast<const uint2*>(src + i * ldx));
+        if constexpr (kPlain) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mp = raw_absmax_acc<T>(mp, raw[i]);
+        }
 #pragma unroll
         for (int pr = 0; pr < kPairs; ++pr) {
             uint64_t v[16];
@@ -219,6 +241,11 @@ __global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* _
     m = __float_as_uint(__fmul_rn(__uint_as_float(m), 0.25f)) & 0x7FFFFFFFu;
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
+    if constexpr (kPlain) {
+        if (sizeof(T) == 2) mp = max(mp & 0xFFFFu, mp >> 16) << 16;  // widen to an FP32 pattern
+        mp = block_max_u32(mp, red);
+        if (threadIdx.x == 0) partials_plain[blockIdx.x] = mp;
+    }
 }
 
 // Pass 1 of the rowwise RHT path (the transform along each row, i.e. along
@@ -822,13 +849,16 @@ void launch_rht_rows_amax(const void* x, bool fp32, int64_t rows, int64_t cols, 
 }
 
 void launch_rht_amax(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx, uint64_t rht_seed,
-                     uint32_t* partials, int grid, cudaStream_t s) {
-    if (fp32)
-        rht_amax_kernel<float><<<grid, kRhtAmaxThreads, 0, s>>>(static_cast<const float*>(x), rows, cols, ldx, rht_seed,
-                                                             partials);
-    else
-        rht_amax_kernel<__nv_bfloat16><<<grid, kRhtAmaxThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows,
-                                                                     cols, ldx, rht_seed, partials);
+                     uint32_t* partials, int grid, cudaStream_t s, uint32_t* partials_plain) {
+#define NVFP4_RHT_AMAX(T, P)                                                                                 \
+    rht_amax_kernel<T, P><<<grid, kRhtAmaxThreads, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx, rht_seed, \
+                                                           partials, partials_plain)
+    if (fp32) {
+        if (partials_plain) NVFP4_RHT_AMAX(float, true); else NVFP4_RHT_AMAX(float, false);
+    } else {
+        if (partials_plain) NVFP4_RHT_AMAX(__nv_bfloat16, true); else NVFP4_RHT_AMAX(__nv_bfloat16, false);
+    }
+#undef NVFP4_RHT_AMAX
 }
 
 void launch_quantize_rowwise(const void* x, bool fp32, int64_t rows, int64_t cols, int64_t ldx,

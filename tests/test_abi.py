@@ -97,6 +97,31 @@ def test_host_argument_checks_need_no_gpu(L):
     assert L.nvfp4_rht_quantize(16, 0, 24, 32, 32, 0, 0, 0, ctypes.byref(tc2), 16, 8192, None) == q.ERR_INVALID_ARG
 
 
+def test_quantize_with_rht_argument_checks_need_no_gpu(L):
+    import quantize_block_scaled_amax_gb300 as q
+    r = q.nvfp4_tensor(16, 16, 16, 32, 64, 32, 1, 0)       # x^T... rowwise [32][64]
+    c = q.nvfp4_tensor(16, 16, 16, 64, 32, 16, 1, 0)       # colwise [64][32]
+    ws = 2 * 8192
+    # both outputs required
+    assert L.nvfp4_quantize_with_rht(16, 0, 32, 64, 64, 0, 0, 0, ctypes.byref(r), None, 16, ws, None) == \
+        q.ERR_INVALID_ARG
+    # rows % 16
+    r24 = q.nvfp4_tensor(16, 16, 16, 24, 64, 32, 1, 0)
+    c24 = q.nvfp4_tensor(16, 16, 16, 64, 24, 16, 1, 0)
+    assert L.nvfp4_quantize_with_rht(16, 0, 24, 64, 64, 0, 0, 0, ctypes.byref(r24), ctypes.byref(c24), 16, ws,
+                                     None) == q.ERR_INVALID_ARG
+    # MXFP4 outputs
+    rm = q.nvfp4_tensor(16, 16, 16, 32, 64, 32, 1, 1)
+    cm = q.nvfp4_tensor(16, 16, 16, 64, 32, 16, 1, 1)
+    assert L.nvfp4_quantize_with_rht(16, 0, 32, 64, 64, 0, 0, 0, ctypes.byref(rm), ctypes.byref(cm), 16, ws,
+                                     None) == q.ERR_INVALID_ARG
+    # 8 KB is enough for the single calls but not for this one
+    assert L.nvfp4_quantize_with_rht(16, 0, 32, 64, 64, 0, 0, 0, ctypes.byref(r), ctypes.byref(c), 16, 8192,
+                                     None) == q.ERR_WORKSPACE
+    assert b"workspace" in L.nvfp4_last_error()
+    assert q.nvfp4_workspace_size() >= ws
+
+
 def test_bf16_gemm_argument_checks_need_no_gpu(L):
     import quantize_block_scaled_amax_gb300 as q
     # K % 8 != 0
