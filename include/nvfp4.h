@@ -283,6 +283,19 @@ nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t 
                              nvfp4_stream_t stream);
 
 /*
+ * nvfp4_transpose_bf16 -- y = x^T for a bf16 x [rows][ldx] into y
+ * [cols][ldy].  Not a step of the method: the BF16 fallback GEMM above takes
+ * K-major operands, and a layer kept in (or switched back to) BF16 needs W^T
+ * for Dgrad and dY^T, X^T for Wgrad.
+ *   rows, cols   positive multiples of 8; ldx >= cols, ldy >= rows, both
+ *                multiples of 8 elements; x and y device, 16-byte aligned,
+ *                not overlapping.
+ *   Errors: NVFP4_ERR_INVALID_ARG for any of the above, before any launch.
+ */
+nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy,
+                                  nvfp4_stream_t stream);
+
+/*
  * Linear layer Y = X W^T with NVFP4 GEMMs, following the recipe (paper
  * page: 2D weight scaling keeps Fprop and Dgrad consistent, Hadamard only on
  * Wgrad; blog: stochastic rounding on gradients):

@@ -21,6 +21,7 @@ from . import build as _build
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
     "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
+    "nvfp4_transpose_bf16",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
@@ -87,6 +88,8 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_rht_quantize.restype = st
             L.nvfp4_rht_quantize.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, vp, ctypes.c_size_t, vp]
             L.nvfp4_rht_quantize_rowwise.restype = st
+            L.nvfp4_transpose_bf16.restype = st
+            L.nvfp4_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, i64, vp]
             L.nvfp4_quantize_with_rht.restype = st
             L.nvfp4_quantize_with_rht.argtypes = [vp, st, i64, i64, i64, st, u64, u64, tp, tp, vp, ctypes.c_size_t,
                                                   vp]
@@ -319,6 +322,19 @@ def nvfp4_gemm_bf16(a: torch.Tensor, b: torch.Tensor, out_dtype=torch.bfloat16, 
     st = lib().nvfp4_gemm_bf16(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), out.data_ptr(), od,
                                out.stride(0), a.shape[0], b.shape[0], a.shape[1], _stream(stream))
     _check(st, "nvfp4_gemm_bf16")
+    return out
+
+
+def nvfp4_transpose_bf16(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """x^T of a 2D row-major bf16 CUDA tensor (rows, cols multiples of 8)."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2D row-major bf16 CUDA tensor")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty(cols, rows, dtype=torch.bfloat16, device=x.device)
+    st = lib().nvfp4_transpose_bf16(x.data_ptr(), rows, cols, x.stride(0), out.data_ptr(), out.stride(0),
+                                    _stream(stream))
+    _check(st, "nvfp4_transpose_bf16")
     return out
 
 

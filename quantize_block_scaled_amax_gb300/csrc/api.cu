@@ -460,6 +460,25 @@ static nvfp4_status check_linear_tensor(const nvfp4_tensor* t, int64_t rows, int
     return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy,
+                                  nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    if (!x || !y) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    if (rows <= 0 || cols <= 0 || rows % 8 || cols % 8)
+        return fail(NVFP4_ERR_INVALID_ARG, "rows and cols must be positive multiples of 8, got %lld x %lld",
+                    (long long)rows, (long long)cols);
+    if (ldx < cols || ldx % 8 || ldy < rows || ldy % 8)
+        return fail(NVFP4_ERR_INVALID_ARG, "ldx (>= cols) and ldy (>= rows) must be multiples of 8 elements");
+    if (!aligned16(x) || !aligned16(y)) return fail(NVFP4_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+    DeviceInfo* dev;
+    nvfp4_status st;
+    if ((st = device_info(&dev))) return st;
+    const int64_t units = (rows / 8) * (cols / 8);
+    const int grid = cap_grid(ceil_div(units, (int64_t)256), 8, dev->num_sms);
+    launch_transpose_bf16(x, rows, cols, ldx, y, ldy, grid, reinterpret_cast<cudaStream_t>(stream));
+    return check_launch("transpose_bf16");
+}
+
 nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
     g_err[0] = 0;
     if (!ctx || !X || !W || !Y) return fail(NVFP4_ERR_INVALID_ARG, "null argument");

@@ -37,6 +37,9 @@ void launch_quantize_2d(const void* x, bool fp32, int64_t rows, int64_t cols, in
                         int64_t ld_c, ScaleOut so_c, float* amax_c, uint32_t* status, int grid, cudaStream_t s);
 int64_t colwise_tiles(int64_t rows, int64_t cols);
 int quantize_2d_grid(int64_t rows, int64_t cols, bool fp32, int num_sms);
+// y[cols][rows] = x^T, bf16; rows, cols % 8 == 0; x, y, ldx, ldy 16-byte granular
+void launch_transpose_bf16(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy, int grid,
+                           cudaStream_t s);
 
 // GEMM (gemm.cu).  A: [M][K] codes/scales (MMA layout), B: [N][K].
 struct GemmArgs {

@@ -824,6 +824,39 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// bf16 transpose, y[c][r] = x[r][c] (the BF16 fallback GEMM takes K-major
+// operands; its Dgrad and Wgrad need W^T, dY^T and X^T).  A thread moves an
+// 8 x 8 block: eight 16-byte row loads (a warp's 32 neighbouring blocks read
+// 512 contiguous bytes per row), one byte permute per output word (word k of
+// output row j holds rows 2k and 2k + 1 of input column j, i.e. halves of
+// input words [2k][j/2] and [2k+1][j/2]) and eight 16-byte stores.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4* __restrict__ x, int64_t rows, int64_t cols,
+                                                            int64_t ldx_vec, uint4* __restrict__ y, int64_t ldy_vec) {
+    const int64_t cb_n = cols / 8;
+    const int64_t nunits = (rows / 8) * cb_n;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nunits; u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t rb = u / cb_n, cb = u - rb * cb_n;
+        uint32_t w[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = __ldg(x + (8 * rb + i) * ldx_vec + cb);
+            w[i][0] = v.x;
+            w[i][1] = v.y;
+            w[i][2] = v.z;
+            w[i][3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;  // high halves : low halves
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __byte_perm(w[2 * k][j / 2], w[2 * k + 1][j / 2], sel);
+            y[(8 * cb + j) * ldy_vec + rb] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launchers.
 
 template <typename T>
@@ -940,6 +973,12 @@ int quantize_2d_grid(int64_t rows, int64_t cols, bool fp32, int num_sms) {
     const int64_t units = ((rows + unit_rows - 1) / unit_rows) * ((cols + 127) / 128);
     const int64_t ctas = (units + k2dThreads / 32 - 1) / (k2dThreads / 32);
     return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)o * num_sms));
+}
+
+void launch_transpose_bf16(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy, int grid,
+                           cudaStream_t s) {
+    transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), rows, cols, ldx / 8,
+                                               static_cast<uint4*>(y), ldy / 8);
 }
 
 }  // namespace nvfp4

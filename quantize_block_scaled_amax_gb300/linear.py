@@ -14,6 +14,15 @@ counter (``seed_base + call index``), so repeated steps do not reuse the
 rounding decisions, and a run started from the same ``seed_base`` repeats
 them exactly.  The RHT sign vector uses ``rht_seed`` (one per layer; both
 Wgrad operands of a call share it, as the transform requires).
+
+Precision: the paper page keeps some linear layers in BF16 (the last blocks
+of the network) and switches the whole model to BF16 for the final part of
+training to close the remaining loss gap.  A layer's ``precision`` is
+"nvfp4" or "bf16"; "bf16" runs the same three GEMMs on bf16 operands with
+the library's BF16 tensor-core GEMM (FP32 accumulation, bf16 results) and
+its transpose kernel for the K-major operands of Dgrad and Wgrad.
+``set_precision(model, "bf16")`` switches every such layer of a model at
+once.
 """
 from __future__ import annotations
 
@@ -21,9 +30,11 @@ import threading
 
 import torch
 
-from . import LinearContext, nvfp4_linear_bwd, nvfp4_linear_fwd
+from . import LinearContext, nvfp4_gemm_bf16, nvfp4_linear_bwd, nvfp4_linear_fwd, nvfp4_transpose_bf16
 
-__all__ = ["NVFP4LinearFunction", "NVFP4Linear", "nvfp4_linear"]
+__all__ = ["NVFP4LinearFunction", "BF16LinearFunction", "NVFP4Linear", "nvfp4_linear", "set_precision"]
+
+PRECISIONS = ("nvfp4", "bf16")
 
 
 class _SeedCounter:
@@ -105,6 +116,36 @@ class NVFP4LinearFunction(torch.autograd.Function):
         return dx.reshape(*ctx.lead, lc.K), dw.to(ctx.w_dtype), None, None, None
 
 
+class BF16LinearFunction(torch.autograd.Function):
+    """Y = X W^T with bf16 operands on the tensor cores (FP32 accumulation):
+    the layers the recipe keeps in high precision.  X [..., K] bf16, W [N, K]
+    bf16; Y, dX and dW are bf16.  M, N, K must be multiples of 8."""
+
+    @staticmethod
+    def forward(ctx, x, w):
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        w = w.contiguous()
+        if x2.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+            raise TypeError(f"BF16 linear takes bf16 X and W, got {x2.dtype} and {w.dtype}")
+        if w.dim() != 2 or x2.shape[1] != w.shape[1]:
+            raise ValueError(f"X [..., K] and W [N, K] disagree: {tuple(x2.shape)} vs {tuple(w.shape)}")
+        if x2.shape[0] % 8 or w.shape[0] % 8 or w.shape[1] % 8:
+            raise ValueError(f"M, N, K must be multiples of 8, got {x2.shape[0]}, {w.shape[0]}, {w.shape[1]}")
+        y = nvfp4_gemm_bf16(x2, w)                          # [M][N] = X W^T
+        ctx.save_for_backward(x2, w)
+        ctx.lead = lead
+        return y.reshape(*lead, w.shape[0])
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, w = ctx.saved_tensors
+        dy2 = dy.reshape(-1, w.shape[0]).to(torch.bfloat16).contiguous()
+        dx = nvfp4_gemm_bf16(dy2, nvfp4_transpose_bf16(w))  # [M][K] = dY W
+        dw = nvfp4_gemm_bf16(nvfp4_transpose_bf16(dy2), nvfp4_transpose_bf16(x2))  # [N][K] = dY^T X
+        return dx.reshape(*ctx.lead, w.shape[1]), dw
+
+
 class NVFP4Linear(torch.nn.Module):
     """A bias-free linear layer whose three GEMMs run in NVFP4 on the tcgen05
     tensor cores.  ``weight`` is a bf16 parameter [out_features, in_features]
@@ -112,10 +153,14 @@ class NVFP4Linear(torch.nn.Module):
     recipe); in_features, out_features and the token count must be multiples
     of 64."""
 
-    def __init__(self, in_features: int, out_features: int, device=None, seed_base: int = 1, rht_seed: int = 2):
+    def __init__(self, in_features: int, out_features: int, device=None, seed_base: int = 1, rht_seed: int = 2,
+                 precision: str = "nvfp4"):
         super().__init__()
         if in_features % 64 or out_features % 64:
             raise ValueError("in_features and out_features must be multiples of 64")
+        if precision not in PRECISIONS:
+            raise ValueError(f"precision must be one of {PRECISIONS}, got {precision!r}")
+        self.precision = precision
         self.weight = torch.nn.Parameter(torch.empty(out_features, in_features, dtype=torch.bfloat16, device=device))
         torch.nn.init.normal_(self.weight, std=0.02)
         self._contexts = _Contexts()
@@ -123,7 +168,26 @@ class NVFP4Linear(torch.nn.Module):
         self.rht_seed = int(rht_seed)
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if self.precision == "bf16":
+            return BF16LinearFunction.apply(x, self.weight)
         return NVFP4LinearFunction.apply(x, self.weight, self._contexts, self._seeds, self.rht_seed)
+
+    def extra_repr(self) -> str:
+        return f"in_features={self.weight.shape[1]}, out_features={self.weight.shape[0]}, precision={self.precision}"
+
+
+def set_precision(module: torch.nn.Module, precision: str) -> int:
+    """Set ``precision`` ("nvfp4" or "bf16") on every NVFP4Linear in
+    ``module`` (itself included), e.g. for the switch to BF16 near the end of
+    training; returns how many layers were set."""
+    if precision not in PRECISIONS:
+        raise ValueError(f"precision must be one of {PRECISIONS}, got {precision!r}")
+    n = 0
+    for m in module.modules():
+        if isinstance(m, NVFP4Linear):
+            m.precision = precision
+            n += 1
+    return n
 
 
 def nvfp4_linear(x: torch.Tensor, w: torch.Tensor, sr_seed: int = 1, rht_seed: int = 2) -> torch.Tensor:

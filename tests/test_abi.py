@@ -122,6 +122,16 @@ def test_quantize_with_rht_argument_checks_need_no_gpu(L):
     assert q.nvfp4_workspace_size() >= ws
 
 
+def test_transpose_argument_checks_need_no_gpu(L):
+    import quantize_block_scaled_amax_gb300 as q
+    assert L.nvfp4_transpose_bf16(None, 8, 8, 8, 16, 8, None) == q.ERR_INVALID_ARG      # null x
+    assert L.nvfp4_transpose_bf16(16, 12, 8, 8, 16, 16, None) == q.ERR_INVALID_ARG     # rows % 8
+    assert L.nvfp4_transpose_bf16(16, 8, 8, 4, 16, 8, None) == q.ERR_INVALID_ARG       # ldx < cols
+    assert L.nvfp4_transpose_bf16(16, 8, 8, 8, 16, 4, None) == q.ERR_INVALID_ARG       # ldy < rows
+    assert L.nvfp4_transpose_bf16(24, 8, 8, 8, 16, 8, None) == q.ERR_INVALID_ARG       # misaligned x
+    assert L.nvfp4_transpose_bf16(16, 8, 8, 8, 0, 8, None) == q.ERR_INVALID_ARG        # null y
+
+
 def test_bf16_gemm_argument_checks_need_no_gpu(L):
     import quantize_block_scaled_amax_gb300 as q
     # K % 8 != 0
