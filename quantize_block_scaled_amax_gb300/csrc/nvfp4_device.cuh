@@ -114,10 +114,18 @@ __device__ __forceinline__ uint32_t e2m1x2_rtn(float lo, float hi) {
     return h & 0xFFu;
 }
 
+// eight values -> one word, v[0] in the lowest nibble (the four converted
+// bytes are packed by one vector move instead of shifts and ORs)
 __device__ __forceinline__ uint32_t e2m1x8_rtn(const float v[8]) {
-    uint32_t out = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) out |= e2m1x2_rtn(v[2 * j], v[2 * j + 1]) << (8 * j);
+    uint32_t out;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(out)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
     return out;
 }
 
