@@ -63,13 +63,41 @@ struct BlockScale {
     float r;      // per-element multiplier S_enc / sb
 };
 
-__device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc) {
+// x / 6 correctly rounded, for x >= 0.  q = x * RN(1/6) is within one ulp of
+// the quotient, the remainder x - 6q is exact in one FMA, and one more FMA
+// q + rem * RN(1/6) gives the correctly rounded quotient (the correction step
+// of Markstein's division, P. Markstein, IBM J. Res. Develop. 34(1), 1990).
+// Checked exhaustively against the IEEE division for every finite x >= 0:
+// equal for all x >= 2^-125; below that the quotient is subnormal and the
+// correction can be off, so those x take the IEEE division.
+__device__ __forceinline__ float div6_rn(float x) {
+    if (__float_as_uint(x) < 0x01000000u) return __fdiv_rn(x, 6.0f);
+    const float inv6 = 0.16666667163372039794921875f;  // RN(1/6)
+    const float q = __fmul_rn(x, inv6);
+    return __fmaf_rn(__fmaf_rn(-q, 6.0f, x), inv6, q);
+}
+
+// The multipliers r = S_enc / e4m3(sb) of a tensor, one per E4M3 code, built
+// by a CTA in shared memory before its first block: r saturates to FLT_MAX
+// where the quotient overflows, and sb = 0 (and the unused NaN code) get 0.
+// Ends with a barrier: every thread of the CTA must call it.
+__device__ __forceinline__ void build_r_table(float* tab, float s_enc) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        float r = 0.0f;
+        if (i > 0 && i < 127) {
+            r = __fdiv_rn(s_enc, e4m3_to_float((uint32_t)i));
+            if (isinf(r)) r = kFltMax;
+        }
+        tab[i] = r;
+    }
+    __syncthreads();
+}
+
+// sb = E4M3_RN_sat(fl(bamax / 6) * S_enc) and its multiplier from the table
+__device__ __forceinline__ BlockScale block_scale(float bamax, float s_enc, const float* r_tab) {
     BlockScale b;
-    float t = __fdiv_rn(bamax, 6.0f);
-    b.sb = e4m3_from_float(__fmul_rn(t, s_enc));
-    float r = __fdiv_rn(s_enc, e4m3_to_float(b.sb));
-    b.r = isinf(r) ? kFltMax : r;
-    if (b.sb == 0u) b.r = 0.0f;
+    b.sb = e4m3_from_float(__fmul_rn(div6_rn(bamax), s_enc));
+    b.r = r_tab[b.sb];
     return b;
 }
 

@@ -260,12 +260,12 @@ __global__ void __launch_bounds__(kQuantThreads) rht_rows_amax_kernel(const T* _
 // ---------------------------------------------------------------------------
 // Quantize one block of 16 values in place into 8 bytes of codes.
 template <bool kSR>
-__device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales& ts, const PhiloxKey& key, uint64_t i0,
-                                                uint32_t& sb_out) {
+__device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales& ts, const float* r_tab,
+                                                const PhiloxKey& key, uint64_t i0, uint32_t& sb_out) {
     float bamax = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) bamax = fmaxf(bamax, fabsf(v[k]));
-    BlockScale bs = block_scale(bamax, ts.s_enc);
+    BlockScale bs = block_scale(bamax, ts.s_enc, r_tab);
     if (!ts.finite) bs.sb = 0u;
     sb_out = bs.sb;
     if (bs.sb == 0u) return make_uint2(0u, 0u);
@@ -374,9 +374,11 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
     const __grid_constant__ PhiloxKey key, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
+    __shared__ float r_tab[128];
     TensorScales ts{};
     if constexpr (!kMX) {
         ts = reduce_partials(partials, npartials, amax_out, status, red);
+        build_r_table(r_tab, ts.s_enc);
     } else if (blockIdx.x == 0 && threadIdx.x == 0) {
         amax_out[0] = 0.0f;  // MXFP4 has no tensor scale
         amax_out[1] = 1.0f;
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
             if constexpr (kMX) {
                 c = mx_encode16<kSR>(v, bm[h], key, i0, status, sb);
             } else {
-                BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc);
+                BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc, r_tab);
                 if (!ts.finite) bs.sb = 0u;
                 sb = bs.sb;
                 if (bs.sb != 0u) {
@@ -463,9 +465,11 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const __grid_constant__ PhiloxKey key, uint64_t rht_seed) {
     __shared__ uint32_t red[33];
     __shared__ __align__(16) T tile[kColTileRows][kColTileCols];
+    __shared__ float r_tab[128];
     TensorScales ts{};
     if constexpr (!kMX) {
         ts = reduce_partials(partials, npartials, amax_out, status, red);
+        build_r_table(r_tab, ts.s_enc);
     } else if (blockIdx.x == 0 && threadIdx.x == 0) {
         amax_out[0] = 0.0f;  // MXFP4 has no tensor scale
         amax_out[1] = 1.0f;
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
                         float v[16];
                         load_chunk(b, v);
                         uint32_t sb;
-                        uint2 c = quantize_block<kSR>(v, ts, key, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
+                        uint2 c = quantize_block<kSR>(v, ts, r_tab, key, (uint64_t)oc * (uint64_t)rows + orow0 + 16 * b, sb);
                         w[2 * b] = c.x;
                         w[2 * b + 1] = c.y;
                         sbs |= sb << (8 * b);
@@ -685,8 +689,10 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
     // while one tile is encoded; fp32 quads are twice as wide, so one buffer
     constexpr bool kPipe = U::kTiles == 2;
     __shared__ uint32_t red[33];
+    __shared__ float r_tab[128];
     float* amax_out = amax_r ? amax_r : amax_c;
     const TensorScales ts = reduce_partials(partials, npartials, amax_out, status, red);
+    build_r_table(r_tab, ts.s_enc);
     if (amax_r && amax_c && blockIdx.x == 0 && threadIdx.x == 0) {
         amax_c[0] = ts.amax;
         amax_c[1] = ts.s_dec;
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
             uint32_t m = Quad<T>::widen(acc);
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            BlockScale bs = block_scale(__uint_as_float(m), ts.s_enc);
+            BlockScale bs = block_scale(__uint_as_float(m), ts.s_enc, r_tab);
             if (!ts.finite) bs.sb = 0u;
             const bool zero = bs.sb == 0u;  // every code of the tile is 0
             const uint64_t r2 = f32x2_pack(bs.r, bs.r);
