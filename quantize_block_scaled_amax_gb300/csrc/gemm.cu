@@ -8,31 +8,39 @@
 // put the linear layers' Fprop/Dgrad/Wgrad on block-scaled FP4 MMA with FP32
 // accumulation; this kernel is that MMA.
 //
-// Tile 128 x 256 (M x N), K staged 256 at a time; one persistent CTA per SM,
-// 16 warps in four warpgroups:
-//   warp 0      producer: A and B code tiles by TMA (128-byte swizzle) into
-//               a 4-stage smem ring (48 KB per stage).
-//   warp 2      scale producer: the stage's block scales (MMA layout: three
+// Tile 128 x 384 (M x N), K staged 256 at a time; one persistent CTA per SM,
+// 16 warps in four warpgroups.  The tile's N is computed by two independent
+// accumulation chains: chain 0 takes B rows 0-255 (N = 256 MMAs into TMEM
+// columns 0-255), chain 1 rows 256-383 (N = 128 into columns 256-383), each
+// issued by its own warp.  Back-to-back MMAs into one accumulator wait on
+// each other (about 275 cycles per M=128 N=256 K=64 MMA on this part, against
+// about 182 cycles of tensor-pipe time), so two chains keep the pipe busier
+// than one; 384 accumulator columns leave TMEM room for two scale slots.
+//   warp 0      producer: A (128 rows) and B (three 128-row boxes) code tiles
+//               by TMA (128-byte swizzle) into a 3-stage smem ring (64 KB
+//               per stage).
+//   warp 2      scale producer: the stage's block scales (MMA layout:
 //               contiguous 2 KB runs of 512-byte atoms, A's 128 rows and B's
-//               two 128-row groups) by bulk copies into a 4-slot ring of its
+//               three 128-row groups) by bulk copies into a 2-slot ring of its
 //               own, whose slots free as soon as the scale writers have read
-//               them, so the scales run ahead of the code tiles.
-//   warp 1      TMEM owner and MMA issuer: four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//               (M=128, N=256, K=64) per stage into one TMEM accumulator.
+//               them.
+//   warp 1      TMEM owner and chain-0 MMA issuer; warp 3 chain-1 issuer:
+//               four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (M=128, K=64) per stage each.
 //   warps 4-7   scale-factor writers, one per TMEM lane quarter: they read
-//               the stage's scale atoms from smem and write them into TMEM
-//               with tcgen05.st (layout at scale_role).  Scale copies through
-//               the tensor pipe (tcgen05.cp) would serialize with the MMAs,
-//               and a TMA box of 256 rows x 16 bytes costs about one cycle
-//               per row of the SM's copy bandwidth, so the scales come as
-//               long contiguous runs.
-//   warps 8-15  epilogue: two warps per lane quarter drain 128 accumulator
-//               columns each with tcgen05.ld, release the accumulator, then
-//               scale by alpha, convert and store through a 1 KB swizzled
-//               smem staging tile with TMA tensor stores.
+//               the stage's scale atoms from smem and write them into one of
+//               two TMEM scale slots with tcgen05.st (layout at scale_role).
+//               Scale copies through the tensor pipe (tcgen05.cp) would
+//               serialize with the MMAs, and a TMA box of 256 rows x 16 bytes
+//               costs about one cycle per row of the SM's copy bandwidth, so
+//               the scales come as long contiguous runs.
+//   warps 8-15  epilogue: two warps per lane quarter drain chain 1 (64
+//               columns each) and release it, store it, then drain chain 0
+//               (128 columns each) and release it; stores scale by alpha,
+//               convert and go through a 1 KB swizzled smem staging tile with
+//               TMA tensor stores.
 // Registers: 128 per thread (512 threads fill the register file); the
-// epilogue holds its 128 accumulator words with a few words spilled.
+// epilogue holds its 128 chain-0 accumulator words with a few words spilled.
 // Every mbarrier wait is bounded: past the limit the waiter records
 // NVFP4_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag and all
 // roles drain out to the final barrier, where TMEM is freed.
@@ -48,44 +56,56 @@ namespace nvfp4 {
 namespace gemm {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 384;            // tile N: chain 0 (256) + chain 1 (128)
+constexpr int kChain0N = 256;
+constexpr int kChain1N = BN - kChain0N;
+constexpr int kBBoxRows = 128;     // B rows per TMA box (a box has at most 256 rows)
+constexpr int kBGroups = BN / 128; // 128-row groups of B per tile
 constexpr int BK = 256;            // K elements per stage
 constexpr int BKB = BK / 2;        // bytes per row per stage (= 128, the swizzle width)
-constexpr int kStages = 4;
+constexpr int kStages = 3;         // code-tile ring (smem)
+constexpr int kSfSlots = 2;        // scale-atom ring (smem)
+constexpr int kTmemSlots = 2;      // scale-factor slots in TMEM
+constexpr int kChains = 2;
 constexpr int kMmaK = 64;          // K per tcgen05.mma (FP4)
 constexpr int kMmaPerStage = BK / kMmaK;
 constexpr int kATileBytes = BM * BKB;      // 16 KB
-constexpr int kBTileBytes = BN * BKB;      // 32 KB
+constexpr int kBTileBytes = BN * BKB;      // 48 KB
 constexpr int kSfAtomBytes = 512;           // 128 rows x 4 K blocks (MMA scale layout)
 constexpr int kSfRunBytes = 4 * kSfAtomBytes;  // one 128-row group, one stage (16 K blocks)
-constexpr int kSfStageBytes = 3 * kSfRunBytes; // A, B rows 0-127, B rows 128-255
-constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfStageBytes;
+constexpr int kSfStageBytes = (1 + kBGroups) * kSfRunBytes; // A, then B's three 128-row groups
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
-constexpr int kStagingBytes = 32 * 32;     // per epilogue warp: 32 rows x 32 bytes
+constexpr int kStagingBytes = 32 * 32;     // one staging tile: 32 rows x 32 bytes
+constexpr int kStagingBufs = 2;            // per epilogue warp, used in turn
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns
+constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns (chain 0: 0-255, chain 1: 256-383)
 constexpr uint32_t kSfaCols = kMmaPerStage * 4;         // 4 columns per MMA
-constexpr uint32_t kSfbCols = kMmaPerStage * 8;         // N = 256: two 128-row groups per MMA
-constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
+constexpr uint32_t kSfb0Cols = kMmaPerStage * 8;        // chain 0, N = 256: two 128-row groups per MMA
+constexpr uint32_t kSfb1Cols = kMmaPerStage * 4;        // chain 1, N = 128: one group per MMA
+constexpr uint32_t kSfColsPerSlot = kSfaCols + kSfb0Cols + kSfb1Cols;
 constexpr uint64_t kTimeoutNs = 4000000000ull;          // 4 s per wait
-static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(kAccCols + kTmemSlots * kSfColsPerSlot <= kTmemCols, "TMEM budget");
+static_assert(kSfColsPerSlot % 4 == 0 && kSfaCols % 4 == 0 && kSfb0Cols % 4 == 0, "TMEM columns 4-aligned");
 
 struct __align__(8) SharedState {
-    uint64_t full[kStages];     // A/B tiles landed (TMA transaction count)
-    uint64_t sf_in[kStages];    // scale atoms of the stage landed (bulk-copy transaction count)
-    uint64_t sf_free[kStages];  // scale atoms of the stage read out of smem (4 scale warps)
-    uint64_t sf_full[kStages];  // scales written to TMEM (4 scale warps)
-    uint64_t empty[kStages];    // MMAs of the stage done (tcgen05.commit)
-    uint64_t acc_full;          // accumulator complete (tcgen05.commit)
-    uint64_t acc_empty;         // accumulator drained (8 epilogue warps)
+    uint64_t full[kStages];             // A/B tiles landed (TMA transaction count)
+    uint64_t empty[kStages];            // MMAs of the stage done (tcgen05.commit, both chains)
+    uint64_t sf_in[kSfSlots];           // scale atoms of the slot landed (bulk-copy transaction count)
+    uint64_t sf_free[kSfSlots];         // scale atoms of the slot read out of smem (4 scale warps)
+    uint64_t sf_full[kTmemSlots];       // scales written to the TMEM slot (4 scale warps)
+    uint64_t tmem_free[kTmemSlots];     // MMAs reading the TMEM slot done (tcgen05.commit, both chains)
+    uint64_t acc_full[kChains];         // chain's accumulator complete (tcgen05.commit)
+    uint64_t acc_empty[kChains];        // chain's accumulator drained (8 epilogue warps)
     uint32_t tmem_base;
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes =
-    1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kStagingBytes + sizeof(SharedState);
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes +
+                              (size_t)kSfSlots * kSfStageBytes + (size_t)kEpiWarps * kStagingBufs * kStagingBytes +
+                              sizeof(SharedState);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -312,11 +332,15 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1u;
             if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+            // every box counts in full: rows past the matrix arrive as zeros
             mbar_arrive_expect_tx(&ss->full[s], kATileBytes + kBTileBytes);
             // a stage is 128 bytes of every row: 256 FP4 codes or 64 bf16 values
             const int kx = kt * (p.bf16 ? 64 : BKB);
             tma_load_2d(sA + s * kATileBytes, tmap_a, &ss->full[s], kx, mb * BM);
-            tma_load_2d(sB + s * kBTileBytes, tmap_b, &ss->full[s], kx, nb * BN);
+#pragma unroll
+            for (int g = 0; g < kBGroups; ++g)
+                tma_load_2d(sB + s * kBTileBytes + g * kBBoxRows * BKB, tmap_b, &ss->full[s], kx,
+                            nb * BN + g * kBBoxRows);
         }
     }
 }
@@ -327,20 +351,19 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
     for (int i = 0; i < S.count(); ++i) {
         int mb, nb;
         S.tile(i, p, mb, nb);
-        const bool b_hi = 2 * nb + 1 < p.b_groups;  // B rows 128..255 of the tile exist
+        // B's 128-row groups of the tile that exist (the scale buffer has none past them)
+        const int ng = min(kBGroups, p.b_groups - kBGroups * nb);
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1u;
-            if (!mbar_wait(&ss->sf_free[s], ph ^ 1u, ss, p.status)) return;
-            uint8_t* sf = sSf + s * kSfStageBytes;
-            mbar_arrive_expect_tx(&ss->sf_in[s], (b_hi ? 3 : 2) * kSfRunBytes);
-            bulk_load(sf, p.a_scales + ((size_t)mb * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes, &ss->sf_in[s]);
-            bulk_load(sf + kSfRunBytes, p.b_scales + ((size_t)(2 * nb) * p.n_katoms + 4 * kt) * kSfAtomBytes,
-                      kSfRunBytes, &ss->sf_in[s]);
-            if (b_hi)
-                bulk_load(sf + 2 * kSfRunBytes,
-                          p.b_scales + ((size_t)(2 * nb + 1) * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes,
-                          &ss->sf_in[s]);
+            const int r = it % kSfSlots;
+            const uint32_t ph = (it / kSfSlots) & 1u;
+            if (!mbar_wait(&ss->sf_free[r], ph ^ 1u, ss, p.status)) return;
+            uint8_t* sf = sSf + r * kSfStageBytes;
+            mbar_arrive_expect_tx(&ss->sf_in[r], (1 + ng) * kSfRunBytes);
+            bulk_load(sf, p.a_scales + ((size_t)mb * p.n_katoms + 4 * kt) * kSfAtomBytes, kSfRunBytes, &ss->sf_in[r]);
+            for (int g = 0; g < ng; ++g)
+                bulk_load(sf + (1 + g) * kSfRunBytes,
+                          p.b_scales + ((size_t)(kBGroups * nb + g) * p.n_katoms + 4 * kt) * kSfAtomBytes,
+                          kSfRunBytes, &ss->sf_in[r]);
         }
     }
 }
@@ -350,50 +373,61 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
 // every MMA (0.40 -> 0.63 ms at 8192x20480x5120).
 enum MmaKind { kNvf4 = 0, kMxf4 = 1, kBf16 = 2 };
 
+// One accumulation chain: chain 0 multiplies A by B rows 0-255 of the tile
+// into TMEM columns 0-255, chain 1 by rows 256-383 into columns 256-383.  Both
+// wait for the same stages and scale slots and commit to the same "empty" and
+// "TMEM slot free" barriers (two arrivals each).
 template <int kKind>
 __device__ __forceinline__ void mma_loop(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
-                                         uint32_t tmem_base) {
+                                         uint32_t tmem_base, int chain) {
     const Sched S(p);
-    const uint32_t idesc = kKind == kBf16 ? instr_desc_bf16(BM, BN) : instr_desc_nvf4(BM, BN, kKind == kMxf4);
+    const int n = chain ? kChain1N : kChain0N;
+    const uint32_t idesc = kKind == kBf16 ? instr_desc_bf16(BM, n) : instr_desc_nvf4(BM, n, kKind == kMxf4);
+    const uint32_t d_tmem = tmem_base + (chain ? (uint32_t)kChain0N : 0u);
+    const uint32_t b_off = chain ? (uint32_t)(kChain0N * BKB) : 0u;  // the chain's first B row in the stage
+    const uint32_t sfb_off = chain ? kSfaCols + kSfb0Cols : kSfaCols;
+    const uint32_t sfb_step = chain ? 4u : 8u;                       // scale columns per MMA
     const uint32_t sf_base = tmem_base + kAccCols;
     uint32_t it = 0, tc = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
-        if (!mbar_wait(&ss->acc_empty, (tc & 1u) ^ 1u, ss, p.status)) return;
+        if (!mbar_wait(&ss->acc_empty[chain], (tc & 1u) ^ 1u, ss, p.status)) return;
         tc_fence_after();
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1u;
+            const int ts = it % kTmemSlots;
             if (!mbar_wait(&ss->full[s], ph, ss, p.status) ||
-                (kKind != kBf16 && !mbar_wait(&ss->sf_full[s], ph, ss, p.status)))
+                (kKind != kBf16 && !mbar_wait(&ss->sf_full[ts], (it / kTmemSlots) & 1u, ss, p.status)))
                 return;
             tc_fence_after();
-            const uint32_t sfa_t = sf_base + s * kSfColsPerStage;
-            const uint32_t sfb_t = sfa_t + kSfaCols;
+            const uint32_t sfa_t = sf_base + ts * kSfColsPerSlot;
+            const uint32_t sfb_t = sfa_t + sfb_off;
             const uint32_t a_s = smem_u32(sA + s * kATileBytes);
-            const uint32_t b_s = smem_u32(sB + s * kBTileBytes);
+            const uint32_t b_s = smem_u32(sB + s * kBTileBytes) + b_off;
 #pragma unroll
             for (int j = 0; j < kMmaPerStage; ++j) {
                 const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
                 const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
                 const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
                 if constexpr (kKind == kBf16)
-                    mma_bf16(tmem_base, adesc, bdesc, idesc, acc);
+                    mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
                 else if constexpr (kKind == kMxf4)
-                    mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
+                    mma_mxf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + sfb_step * j, acc);
                 else
-                    mma_nvf4(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
+                    mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + sfb_step * j, acc);
             }
             mma_commit(&ss->empty[s]);
+            if constexpr (kKind != kBf16) mma_commit(&ss->tmem_free[ts]);
         }
-        mma_commit(&ss->acc_full);
+        mma_commit(&ss->acc_full[chain]);
     }
 }
 
 __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* sA, uint8_t* sB,
-                                         uint32_t tmem_base) {
-    if (p.bf16) mma_loop<kBf16>(p, ss, sA, sB, tmem_base);
-    else if (p.mx) mma_loop<kMxf4>(p, ss, sA, sB, tmem_base);
-    else mma_loop<kNvf4>(p, ss, sA, sB, tmem_base);
+                                         uint32_t tmem_base, int chain) {
+    if (p.bf16) mma_loop<kBf16>(p, ss, sA, sB, tmem_base, chain);
+    else if (p.mx) mma_loop<kMxf4>(p, ss, sA, sB, tmem_base, chain);
+    else mma_loop<kNvf4>(p, ss, sA, sB, tmem_base, chain);
 }
 
 // Scale-factor TMEM layout read by one MMA (measured on the hardware):
@@ -417,20 +451,21 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
     for (int i = 0; i < S.count(); ++i) {
         int mb, nb;
         S.tile(i, p, mb, nb);
-        const bool b_hi = 2 * nb + 1 < p.b_groups;
+        const int ng = min(kBGroups, p.b_groups - kBGroups * nb);  // B groups that exist
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1u;
-            if (!warp_wait(&ss->sf_in[s], ph, ss, p.status)) return;
-            const uint8_t* sf = sSf + s * kSfStageBytes + lane * 16;
+            const int r = it % kSfSlots;
+            const int ts = it % kTmemSlots;
+            if (!warp_wait(&ss->sf_in[r], (it / kSfSlots) & 1u, ss, p.status)) return;
+            const uint8_t* sf = sSf + r * kSfStageBytes + lane * 16;
             uint32_t wa[kMmaPerStage];
-            uint4 wb[2][kMmaPerStage];
+            uint4 wb[kBGroups][kMmaPerStage];
 #pragma unroll
             for (int j = 0; j < kMmaPerStage; ++j) {
                 wa[j] = *reinterpret_cast<const uint32_t*>(sf + j * kSfAtomBytes + 4 * q);
-                wb[0][j] = *reinterpret_cast<const uint4*>(sf + kSfRunBytes + j * kSfAtomBytes);
-                wb[1][j] = b_hi ? *reinterpret_cast<const uint4*>(sf + 2 * kSfRunBytes + j * kSfAtomBytes)
-                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int g = 0; g < kBGroups; ++g)
+                    wb[g][j] = g < ng ? *reinterpret_cast<const uint4*>(sf + (1 + g) * kSfRunBytes + j * kSfAtomBytes)
+                                      : make_uint4(0u, 0u, 0u, 0u);
             }
             if (p.mx) {
                 // MXFP4 stores each 32-element block's scale in both of its
@@ -439,21 +474,23 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
 #pragma unroll
                 for (int j = 0; j < kMmaPerStage; ++j) {
                     wa[j] = __byte_perm(wa[j], 0u, 0x4420);
-                    wb[0][j] = make_uint4(__byte_perm(wb[0][j].x, 0u, 0x4420), __byte_perm(wb[0][j].y, 0u, 0x4420),
-                                          __byte_perm(wb[0][j].z, 0u, 0x4420), __byte_perm(wb[0][j].w, 0u, 0x4420));
-                    wb[1][j] = make_uint4(__byte_perm(wb[1][j].x, 0u, 0x4420), __byte_perm(wb[1][j].y, 0u, 0x4420),
-                                          __byte_perm(wb[1][j].z, 0u, 0x4420), __byte_perm(wb[1][j].w, 0u, 0x4420));
+#pragma unroll
+                    for (int g = 0; g < kBGroups; ++g)
+                        wb[g][j] = make_uint4(__byte_perm(wb[g][j].x, 0u, 0x4420), __byte_perm(wb[g][j].y, 0u, 0x4420),
+                                              __byte_perm(wb[g][j].z, 0u, 0x4420), __byte_perm(wb[g][j].w, 0u, 0x4420));
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ss->sf_free[s]);
-            // the TMEM slot is free once the MMAs that read it four stages ago are done
-            if (!warp_wait(&ss->empty[s], ph ^ 1u, ss, p.status)) return;
+            if (lane == 0) mbar_arrive(&ss->sf_free[r]);
+            // the TMEM slot is free once both chains' MMAs that read it
+            // kTmemSlots stages ago are done
+            if (!warp_wait(&ss->tmem_free[ts], ((it / kTmemSlots) & 1u) ^ 1u, ss, p.status)) return;
             tc_fence_after();
-            const uint32_t col = lane_addr + sf_base + s * kSfColsPerStage;
+            const uint32_t col = lane_addr + sf_base + ts * kSfColsPerSlot;
             const uint32_t va[16] = {wa[0], wa[0], wa[0], wa[0], wa[1], wa[1], wa[1], wa[1],
                                      wa[2], wa[2], wa[2], wa[2], wa[3], wa[3], wa[3], wa[3]};
             tmem_st_x16(col, va);
+            // chain 0 (B rows 0-255): 8 columns per MMA, groups 0 and 1
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // MMAs 2h and 2h + 1
                 uint32_t vb[16];
@@ -465,85 +502,118 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
                 }
                 tmem_st_x16(col + kSfaCols + 16 * h, vb);
             }
+            // chain 1 (B rows 256-383): 4 columns per MMA, group 2
+            {
+                uint32_t vc[16];
+#pragma unroll
+                for (int j = 0; j < kMmaPerStage; ++j) {
+                    vc[4 * j + 0] = wb[2][j].x; vc[4 * j + 1] = wb[2][j].y;
+                    vc[4 * j + 2] = wb[2][j].z; vc[4 * j + 3] = wb[2][j].w;
+                }
+                tmem_st_x16(col + kSfaCols + kSfb0Cols, vc);
+            }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ss->sf_full[s]);
+            if (lane == 0) mbar_arrive(&ss->sf_full[ts]);
         }
     }
 }
 
-// Epilogue warp e: lane quarter q = warp % 4, accumulator half h (columns
-// [128h, 128h + 128)).  Rows leave through a 32 x 32-byte staging tile in
-// the 32-byte swizzle (16-byte chunk j of row r at position j ^ ((r/4) % 2)),
-// one TMA store per 32 bytes of every row.
+// Stores NC accumulator columns of the lane's row (this warp's 32 rows of
+// C, starting at column col0): scale by alpha, convert, and write through
+// the warp's two 32 x 32-byte staging tiles in turn (32-byte swizzle: 16-byte
+// chunk j of row r at position j ^ ((r/4) % 2)), one TMA store per 32 bytes
+// of every row.  Every chunk commits one bulk group (empty if its store is
+// skipped), so waiting until at most one group is still reading smem frees
+// the tile the chunk before last used; `chunk` counts the warp's chunks.
+template <int NC>
+__device__ __forceinline__ void store_cols(const CUtensorMap* tmap_c, const Params& p, const uint32_t (&acc)[NC],
+                                           float alpha, uint8_t* stage, int sw, int lane, int col0, int y,
+                                           bool rows_in, uint32_t& chunk) {
+    constexpr int kPerChunk32 = 8;  // fp32 columns per 32-byte row
+    constexpr int kPerChunk16 = 16; // bf16 columns per 32-byte row
+    const bool f32 = p.out_fp32 != 0;
+    const int per = f32 ? kPerChunk32 : kPerChunk16;
+#pragma unroll
+    for (int c = 0; c < NC / kPerChunk32; ++c) {
+        if (!f32 && c >= NC / kPerChunk16) break;
+        uint8_t* buf = stage + (chunk & 1u) * kStagingBytes;
+        uint8_t* row_base = buf + lane * 32;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint4 v;
+            if (f32) {
+                const uint32_t* a = acc + 8 * c + 4 * j;
+                v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
+                               __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
+                               __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
+                               __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
+            } else {
+                const uint32_t* a = acc + (16 * c + 8 * j) % NC;  // c < NC / 16 here
+                v = make_uint4(
+                    pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
+                    pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
+                    pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
+                    pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
+            }
+            *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            if (rows_in && col0 + per * c < p.N) tma_store_2d(tmap_c, buf, col0 + per * c, y);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        ++chunk;
+    }
+}
+
+// Epilogue warp e: lane quarter q = warp % 4, half h = e / 4.  Per tile it
+// drains chain 1 first (columns 256 + 64h .. +63, released before they are
+// stored), then chain 0 (columns 128h .. +127): at most 128 accumulator
+// words are live at a time.
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
                                               uint8_t* stage, uint32_t tmem_base, int q, int h, int lane) {
     const Sched S(p);
     const float alpha = p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
-    const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
-    uint8_t* row_base = stage + lane * 32;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(32 * q) << 16);
     const int sw = (lane >> 2) & 1;
-    uint32_t tc = 0;
+    uint32_t tc = 0, chunk = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
         int mb, nb;
         S.tile(i, p, mb, nb);
-        if (!warp_wait(&ss->acc_full, tc & 1u, ss, p.status)) break;
-        tc_fence_after();
-        uint32_t acc[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, acc + 32 * c);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ss->acc_empty);
-
         const int y = mb * BM + 32 * q;
-        const int col0 = nb * BN + 128 * h;
         const bool rows_in = y < p.M;
-        if (p.out_fp32) {
+        {
+            if (!warp_wait(&ss->acc_full[1], tc & 1u, ss, p.status)) break;
+            tc_fence_after();
+            uint32_t acc1[kChain1N / 2];
+            const uint32_t t1 = t_lane + (uint32_t)(kChain0N + (kChain1N / 2) * h);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {  // 8 floats per 32-byte row
-                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                __syncwarp();
+            for (int c = 0; c < kChain1N / 64; ++c) tmem_ld_32x32b_x32(t1 + 32 * c, acc1 + 32 * c);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss->acc_empty[1]);
+            store_cols<kChain1N / 2>(tmap_c, p, acc1, alpha, stage, sw, lane,
+                                     nb * BN + kChain0N + (kChain1N / 2) * h, y, rows_in, chunk);
+        }
+        {
+            if (!warp_wait(&ss->acc_full[0], tc & 1u, ss, p.status)) break;
+            tc_fence_after();
+            uint32_t acc0[kChain0N / 2];
+            const uint32_t t0 = t_lane + (uint32_t)((kChain0N / 2) * h);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t* a = acc + 8 * c + 4 * j;
-                    const uint4 v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
-                                               __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
-                                               __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
-                                               __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
-                    *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0 && rows_in && col0 + 8 * c < p.N) {
-                    tma_store_2d(tmap_c, stage, col0 + 8 * c, y);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                }
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16 bf16 per 32-byte row
-                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t* a = acc + 16 * c + 8 * j;
-                    const uint4 v = make_uint4(
-                        pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
-                        pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
-                        pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
-                        pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
-                    *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0 && rows_in && col0 + 16 * c < p.N) {
-                    tma_store_2d(tmap_c, stage, col0 + 16 * c, y);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                }
-            }
+            for (int c = 0; c < kChain0N / 64; ++c) tmem_ld_32x32b_x32(t0 + 32 * c, acc0 + 32 * c);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss->acc_empty[0]);
+            store_cols<kChain0N / 2>(tmap_c, p, acc0, alpha, stage, sw, lane, nb * BN + (kChain0N / 2) * h,
+                                     y, rows_in, chunk);
         }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -558,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = sA + kStages * kATileBytes;
     uint8_t* sSf = sB + kStages * kBTileBytes;
-    uint8_t* sStage = sSf + kStages * kSfStageBytes;
-    SharedState* ss = reinterpret_cast<SharedState*>(sStage + kEpiWarps * kStagingBytes);
+    uint8_t* sStage = sSf + kSfSlots * kSfStageBytes;
+    SharedState* ss = reinterpret_cast<SharedState*>(sStage + kEpiWarps * kStagingBufs * kStagingBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -567,13 +637,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ss->full[s], 1);
-            mbar_init(&ss->sf_in[s], 1);
-            mbar_init(&ss->sf_free[s], kSfWarps);
-            mbar_init(&ss->sf_full[s], kSfWarps);
-            mbar_init(&ss->empty[s], 1);
+            mbar_init(&ss->empty[s], kChains);
         }
-        mbar_init(&ss->acc_full, 1);
-        mbar_init(&ss->acc_empty, kEpiWarps);
+        for (int r = 0; r < kSfSlots; ++r) {
+            mbar_init(&ss->sf_in[r], 1);
+            mbar_init(&ss->sf_free[r], kSfWarps);
+        }
+        for (int t = 0; t < kTmemSlots; ++t) {
+            mbar_init(&ss->sf_full[t], kSfWarps);
+            mbar_init(&ss->tmem_free[t], kChains);
+        }
+        for (int c = 0; c < kChains; ++c) {
+            mbar_init(&ss->acc_full[c], 1);
+            mbar_init(&ss->acc_empty[c], kEpiWarps);
+        }
         ss->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
@@ -596,14 +673,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, sA, sB);
         } else if (warp == 2) {
             if (lane == 0 && !p.bf16) scale_producer_role(p, ss, sSf);
-        } else if (warp == 1) {
-            if (lane == 0) mma_role(p, ss, sA, sB, tmem_base);
+        } else if (warp == 1 || warp == 3) {  // chain 0, chain 1
+            if (lane == 0) mma_role(p, ss, sA, sB, tmem_base, warp == 3 ? 1 : 0);
         } else if (warp >= 4) {
             if (!p.bf16) scale_role(p, ss, sSf, tmem_base, warp & 3, lane);
         }
     } else {
         const int e = warp - 8;
-        epilogue_role(&tmap_c, p, ss, sStage + e * kStagingBytes, tmem_base, warp & 3, e >> 2, lane);
+        epilogue_role(&tmap_c, p, ss, sStage + e * kStagingBufs * kStagingBytes, tmem_base, warp & 3, e >> 2, lane);
     }
 
     // Drain: every role reaches this barrier, then warp 1 frees TMEM.
@@ -670,7 +747,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.M, g.K / 2, g.lda, BKB, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg))
         return 1;
-    if (make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, BN,
+    if (make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, kBBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg))
         return 1;
     if (g.out_fp32) {
@@ -727,7 +804,7 @@ int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
     CUtensorMap ta, tb, tcm;
     if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, g.M, g.K, g.lda * 2, 64, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg) ||
-        make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.b, g.N, g.K, g.ldb * 2, 64, BN,
+        make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.b, g.N, g.K, g.ldb * 2, 64, kBBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B, msg))
         return 1;
     if (g.out_fp32) {
