@@ -21,7 +21,7 @@ def nv():
 
 
 @pytest.mark.parametrize("mnk", [(128, 256, 64), (200, 136, 200), (64, 1000, 8), (1000, 48, 128),
-                                 (384, 512, 1024), (256, 256, 4096)])
+                                 (384, 512, 1024), (256, 256, 4096), (128, 320, 64), (96, 712, 40)])
 def test_bf16_gemm(nv, mnk):
     m, n, k = mnk
     a = workloads.normal_with_outliers(m, k, p=0.005, factor=20.0, seed=m + 7 * k, dtype=torch.bfloat16)

@@ -47,8 +47,12 @@ def test_tiny_config(nv, a_round):
     assert_gemm_close(c16.float().cpu().numpy(), ref, ad, bd, bf16=True, what="tiny bf16")
 
 
+# N against the 384-column tile (chain 0: columns 0-255, chain 1: 256-383):
+# chain 1 out of range (128, 136, 256, 48), partly in range (320, 704: 384 +
+# 320), whole tiles (384), a ragged last tile of two (512) and of three (1000)
 @pytest.mark.parametrize("mnk", [(128, 128, 64), (128, 128, 256), (200, 136, 320), (384, 512, 1024),
-                                 (64, 1000, 512), (1000, 48, 128), (256, 256, 4096)])
+                                 (64, 1000, 512), (1000, 48, 128), (256, 256, 4096), (128, 320, 256),
+                                 (256, 384, 512), (130, 704, 192)])
 def test_shapes(nv, mnk):
     m, n, k = mnk
     a = workloads.normal_with_outliers(m, k, p=0.005, factor=20.0, seed=m + k, dtype=torch.bfloat16)
