@@ -250,26 +250,63 @@ __device__ __forceinline__ uint2 encode16(const float v[16], const PhiloxKey& ke
 }
 
 // ---------------------------------------------------------------------------
+// Packed FP32x2 operations on a register pair (lane 0 in the low word): each
+// lane is the correctly rounded FP32 operation.
+__device__ __forceinline__ uint64_t x2_pack(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float x2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float x2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
+__device__ __forceinline__ uint64_t x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // 16-point random Hadamard transform of one chunk, in place:
 // y = (1/4) H16 (d . x), stages over index bits 0, 1, 2, 3, each sum rounded.
-// `dmask` bit j set means d_j = -1.
+// `dmask` bit j set means d_j = -1.  Stage 0 pairs neighbours (j, j + 1);
+// stages 1-3 pair (j, j + h) with h even, so they run on packed pairs
+// (x[j], x[j + 1]) against (x[j + h], x[j + h + 1]), as does the x1/4: the same
+// correctly rounded operations, half the instructions.
 __device__ __forceinline__ void rht16(float x[16], uint32_t dmask) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
         if ((dmask >> j) & 1u) x[j] = -x[j];
+    uint64_t p[8];  // p[k] = (x[2k], x[2k + 1])
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        const int h = 1 << s;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (j & h) continue;
-            float a = x[j], b = x[j + h];
-            x[j] = __fadd_rn(a, b);
-            x[j + h] = __fsub_rn(a, b);
-        }
+    for (int k = 0; k < 8; ++k) {
+        const float a = x[2 * k], b = x[2 * k + 1];
+        p[k] = x2_pack(__fadd_rn(a, b), __fsub_rn(a, b));  // stage 0
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], 0.25f);
+    for (int s = 1; s < 4; ++s) {
+        const int hp = 1 << (s - 1);  // stride in pairs
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k & hp) continue;
+            const uint64_t a = p[k], b = p[k + hp];
+            p[k] = x2_add(a, b);
+            p[k + hp] = x2_sub(a, b);
+        }
+    }
+    const uint64_t quarter = x2_pack(0.25f, 0.25f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint64_t y = x2_mul(p[k], quarter);
+        x[2 * k] = x2_lo(y);
+        x[2 * k + 1] = x2_hi(y);
+    }
 }
 
 __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t rht_seed) {
