@@ -157,6 +157,41 @@ __device__ __forceinline__ uint32_t e2m1x8_rtn(const float v[8]) {
     return out;
 }
 
+// ---------------------------------------------------------------------------
+// Packed FP32x2 operations on a register pair (lane 0 in the low word): each
+// lane is the correctly rounded FP32 operation.
+__device__ __forceinline__ uint64_t x2_pack(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float x2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float x2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
+__device__ __forceinline__ uint64_t x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t x2_add_rp(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_fma_rp(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // E2M1 stochastic rounding of one value v with its 32-bit random word w, as
 // the grid value it rounds to (sign kept).  The contract: with a = min(|v|, 6),
 // lo <= a < hi the neighbouring grid points, frac = (a - lo) / (hi - lo) and
@@ -183,6 +218,21 @@ __device__ __forceinline__ float e2m1_sr_value(float v, uint32_t w) {
     const float m = __fmul_rn(p, 6291456.0f);  // 1.5 * 2^22 * p = 1.5 * 2^23 * s
     const float y = __fsub_rn(__fadd_ru(z, m), m);
     return __uint_as_float(__float_as_uint(y) | (__float_as_uint(v) & 0x80000000u));
+}
+
+// e2m1_sr_value of two values at once: the FP steps on packed pairs (each
+// lane the same correctly rounded operation, directed roundings included).
+__device__ __forceinline__ void e2m1_sr_pair(float v0, float v1, uint32_t w0, uint32_t w1, float& y0, float& y1) {
+    const uint64_t p = x2_pack(fmaxf(__uint_as_float(__float_as_uint(v0) & 0x7F800000u), 1.0f),
+                               fmaxf(__uint_as_float(__float_as_uint(v1) & 0x7F800000u), 1.0f));
+    const uint64_t uf = x2_pack(__uint2float_rn(w0 & 0xFFFFFF00u), __uint2float_rn(w1 & 0xFFFFFF00u));
+    const uint64_t a = x2_pack(fabsf(v0), fabsf(v1));
+    const float c = -1.16415321826934814453125e-10f;  // -2^-33
+    const uint64_t z = x2_fma_rp(uf, x2_mul(p, x2_pack(c, c)), a);
+    const uint64_t m = x2_mul(p, x2_pack(6291456.0f, 6291456.0f));
+    const uint64_t y = x2_sub(x2_add_rp(z, m), m);
+    y0 = __uint_as_float(__float_as_uint(x2_lo(y)) | (__float_as_uint(v0) & 0x80000000u));
+    y1 = __uint_as_float(__float_as_uint(x2_hi(y)) | (__float_as_uint(v1) & 0x80000000u));
 }
 
 // ---------------------------------------------------------------------------
@@ -238,39 +288,13 @@ __device__ __forceinline__ uint2 encode16(const float v[16], const PhiloxKey& ke
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const uint4 r = sr_words(key, i0 + 4 * q);
-            y[4 * q + 0] = e2m1_sr_value(v[4 * q + 0], r.x);
-            y[4 * q + 1] = e2m1_sr_value(v[4 * q + 1], r.y);
-            y[4 * q + 2] = e2m1_sr_value(v[4 * q + 2], r.z);
-            y[4 * q + 3] = e2m1_sr_value(v[4 * q + 3], r.w);
+            e2m1_sr_pair(v[4 * q + 0], v[4 * q + 1], r.x, r.y, y[4 * q + 0], y[4 * q + 1]);
+            e2m1_sr_pair(v[4 * q + 2], v[4 * q + 3], r.z, r.w, y[4 * q + 2], y[4 * q + 3]);
         }
         out.x = e2m1x8_rtn(y);  // exact: every y is a grid value
         out.y = e2m1x8_rtn(y + 8);
     }
     return out;
-}
-
-// ---------------------------------------------------------------------------
-// Packed FP32x2 operations on a register pair (lane 0 in the low word): each
-// lane is the correctly rounded FP32 operation.
-__device__ __forceinline__ uint64_t x2_pack(float lo, float hi) {
-    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-__device__ __forceinline__ float x2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
-__device__ __forceinline__ float x2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
-__device__ __forceinline__ uint64_t x2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t x2_sub(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t x2_mul(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
 }
 
 // 16-point random Hadamard transform of one chunk, in place:
