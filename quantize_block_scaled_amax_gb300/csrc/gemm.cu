@@ -70,7 +70,7 @@ constexpr int kChains = 2;
 constexpr int kMmaK = 64;          // K per tcgen05.mma (FP4)
 constexpr int kMmaPerStage = BK / kMmaK;
 constexpr int kATileBytes = BM * BKB;      // 16 KB
-constexpr int kBTileBytes = BN * BKB;      // 48 KB
+constexpr int kBTileBytes = BN * BKB;      // 48 KB (three 128-row boxes)
 constexpr int kSfAtomBytes = 512;           // 128 rows x 4 K blocks (MMA scale layout)
 constexpr int kSfRunBytes = 4 * kSfAtomBytes;  // one 128-row group, one stage (16 K blocks)
 constexpr int kSfStageBytes = (1 + kBGroups) * kSfRunBytes; // A, then B's three 128-row groups
@@ -433,15 +433,16 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
 // Scale-factor TMEM layout read by one MMA (measured on the hardware):
 //   A (128 rows): row r at lane r, column base + r/32 -- each lane quarter
 //     reads only its own rows, so lane r holds only its own row's word;
-//   B (256 rows): every lane quarter reads all of B: row n at lane
+//   B (N rows): every lane quarter reads all of B: row n at lane
 //     32q + n%32, column base + n/32, the same in all four quarters.
 // Writer warp q (lanes 32q .. 32q+31 of TMEM), lane l: A row 32q + l, and B
-// rows 32c + l for c = 0..7.  Per stage, MMA j reads A words at columns
-// 4j..4j+3 (the lane's word is written into all four) and B words at
-// 8j..8j+7.  In smem, atom j of a 128-row group holds row 32c + l's four
-// scales of MMA j at byte 16 l + 4 c, so lane l reads A's word with one
-// 4-byte load per MMA and four B words (c = 0..3 of a group) with one
-// 16-byte load per group and MMA.
+// rows 32c + l of the tile.  Per stage and slot, MMA j reads A words at
+// columns 4j..4j+3 (the lane's word is written into all four), chain 0's B
+// words (tile rows 0-255) at 16 + 8j .. 16 + 8j + 7 and chain 1's (rows
+// 256-383) at 48 + 4j .. 48 + 4j + 3.  In smem, atom j of a 128-row group
+// holds row 32c + l's four scales of MMA j at byte 16 l + 4 c, so lane l
+// reads A's word with one 4-byte load per MMA and four B words (c = 0..3 of
+// a group) with one 16-byte load per group and MMA.
 __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, const uint8_t* sSf, uint32_t tmem_base,
                                            int q, int lane) {
     const Sched S(p);
