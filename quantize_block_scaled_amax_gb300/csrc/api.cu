@@ -143,6 +143,14 @@ int amax_grid(int64_t rows, int64_t cols, int64_t ldx, bool fp32, int num_sms) {
     return (int)std::max<int64_t>(g, 1);
 }
 
+// CTAs per SM of the rowwise quantizer.  Every CTA first reduces the amax
+// partials and builds its scale table.  With RTN an item is cheap, so that
+// start-up dominates a CTA's work: launching only what fits on an SM at once
+// (4 CTAs of 256 threads at 64 registers) does it once per resident CTA.
+// With SR the items are heavy and many smaller waves balance the SMs better
+// (4 CTAs per SM measured slower there).
+int row_ctas_per_sm(bool sr) { return sr ? 16 : 4; }
+
 int cap_grid(int64_t units, int per_sm, int num_sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)num_sms * per_sm));
 }
@@ -238,7 +246,7 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
     }
     if (out_rowwise) {
         const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
-        const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
+        const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), row_ctas_per_sm(sr), dev->num_sms);
         launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
                                 scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, mx, seed, false, 0, g,
                                 s);
@@ -319,7 +327,7 @@ nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_
     launch_rht_amax(x, fp32, rows, cols, ldx, rht_seed, partials_rht, ag, s, partials_plain);
     if ((st = check_launch("rht_amax"))) return st;
     const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
-    const int gr = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
+    const int gr = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), row_ctas_per_sm(sr), dev->num_sms);
     launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials_plain, ag, out_rowwise->codes, out_rowwise->ld_codes,
                             scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, false, seed, false, 0, gr, s);
     if ((st = check_launch("quantize_rowwise"))) return st;
@@ -358,7 +366,8 @@ nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int
         launch_rht_rows_amax(x, fp32, rows, cols, ldx, rht_seed, partials, ag, s);
         if ((st = check_launch("rht_rows_amax"))) return st;
     }
-    const int g = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), 16, dev->num_sms);
+    const int g =
+        cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), row_ctas_per_sm(round == NVFP4_SR), dev->num_sms);
     launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials, ag, out_rowwise->codes, out_rowwise->ld_codes,
                             scale_out(*out_rowwise), out_rowwise->amax, dev->status, round == NVFP4_SR, mx, seed,
                             true, rht_seed, g, s);
