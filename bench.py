@@ -21,6 +21,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -106,7 +107,8 @@ class ClockSampler:
             self.proc = None
 
     def _path(self):
-        d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+        # the raw samples; the JSON line carries their summary
+        d = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
         return os.path.join(d, f"bench_clocks_{os.getpid()}.csv")
 
     def stop(self):
