@@ -523,52 +523,66 @@ __device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, con
 
 // Stores NC accumulator columns of the lane's row (this warp's 32 rows of
 // C, starting at column col0): scale by alpha, convert, and write through
-// the warp's two 32 x 32-byte staging tiles in turn (32-byte swizzle: 16-byte
-// chunk j of row r at position j ^ ((r/4) % 2)), one TMA store per 32 bytes
-// of every row.  Every chunk commits one bulk group (empty if its store is
-// skipped), so waiting until at most one group is still reading smem frees
-// the tile the chunk before last used; `chunk` counts the warp's chunks.
+// the warp's two 32 x 32-byte staging tiles (32-byte swizzle: 16-byte chunk
+// j of row r at position j ^ ((r/4) % 2)), one TMA store per 32 bytes of
+// every row.  Chunks go in pairs, one per tile: both are converted in
+// registers, the warp waits until its earlier stores have finished reading
+// both tiles, writes them, fences once and commits the two stores as one
+// bulk group.  NC / 8 (fp32) and NC / 16 (bf16) are even.
 template <int NC>
 __device__ __forceinline__ void store_cols(const CUtensorMap* tmap_c, const Params& p, const uint32_t (&acc)[NC],
                                            float alpha, uint8_t* stage, int sw, int lane, int col0, int y,
-                                           bool rows_in, uint32_t& chunk) {
+                                           bool rows_in) {
     constexpr int kPerChunk32 = 8;  // fp32 columns per 32-byte row
     constexpr int kPerChunk16 = 16; // bf16 columns per 32-byte row
+    static_assert(kStagingBufs == 2 && (NC / kPerChunk32) % 2 == 0 && (NC / kPerChunk16) % 2 == 0,
+                  "chunks are stored in pairs");
     const bool f32 = p.out_fp32 != 0;
     const int per = f32 ? kPerChunk32 : kPerChunk16;
 #pragma unroll
-    for (int c = 0; c < NC / kPerChunk32; ++c) {
-        if (!f32 && c >= NC / kPerChunk16) break;
-        uint8_t* buf = stage + (chunk & 1u) * kStagingBytes;
-        uint8_t* row_base = buf + lane * 32;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    for (int pc = 0; pc < NC / kPerChunk32 / 2; ++pc) {
+        const int c2 = 2 * pc;
+        if (!f32 && c2 >= NC / kPerChunk16) break;
+        uint4 v[2][2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int c = c2 + b;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (f32) {
+                    const uint32_t* a = acc + 8 * c + 4 * j;
+                    v[b][j] = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
+                                         __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
+                                         __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
+                                         __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
+                } else {
+                    const uint32_t* a = acc + (16 * c + 8 * j) % NC;  // c < NC / 16 here
+                    v[b][j] = make_uint4(
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
+                        pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
+                }
+            }
+        }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint4 v;
-            if (f32) {
-                const uint32_t* a = acc + 8 * c + 4 * j;
-                v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
-                               __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
-                               __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
-                               __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
-            } else {
-                const uint32_t* a = acc + (16 * c + 8 * j) % NC;  // c < NC / 16 here
-                v = make_uint4(
-                    pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
-                    pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
-                    pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
-                    pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
-            }
-            *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v;
+        for (int b = 0; b < 2; ++b) {
+            uint8_t* row_base = stage + b * kStagingBytes + lane * 32;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) *reinterpret_cast<uint4*>(row_base + ((j ^ sw) << 4)) = v[b][j];
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-            if (rows_in && col0 + per * c < p.N) tma_store_2d(tmap_c, buf, col0 + per * c, y);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int x = col0 + per * (c2 + b);
+                if (rows_in && x < p.N) tma_store_2d(tmap_c, stage + b * kStagingBytes, x, y);
+            }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
-        ++chunk;
     }
 }
 
@@ -582,7 +596,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
     const float alpha = p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
     const uint32_t t_lane = tmem_base + ((uint32_t)(32 * q) << 16);
     const int sw = (lane >> 2) & 1;
-    uint32_t tc = 0, chunk = 0;
+    uint32_t tc = 0;
     for (int i = 0; i < S.count(); ++i, ++tc) {
         int mb, nb;
         S.tile(i, p, mb, nb);
@@ -600,7 +614,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
             __syncwarp();
             if (lane == 0) mbar_arrive(&ss->acc_empty[1]);
             store_cols<kChain1N / 2>(tmap_c, p, acc1, alpha, stage, sw, lane,
-                                     nb * BN + kChain0N + (kChain1N / 2) * h, y, rows_in, chunk);
+                                     nb * BN + kChain0N + (kChain1N / 2) * h, y, rows_in);
         }
         {
             if (!warp_wait(&ss->acc_full[0], tc & 1u, ss, p.status)) break;
@@ -614,7 +628,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
             __syncwarp();
             if (lane == 0) mbar_arrive(&ss->acc_empty[0]);
             store_cols<kChain0N / 2>(tmap_c, p, acc0, alpha, stage, sw, lane, nb * BN + (kChain0N / 2) * h,
-                                     y, rows_in, chunk);
+                                     y, rows_in);
         }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
