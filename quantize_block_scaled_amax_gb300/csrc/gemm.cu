@@ -265,16 +265,24 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
+// 64 accumulator columns of the warp's 32 lanes, returned only once the
+// load has completed: the load and its wait are one statement, so no use of
+// the registers (a spill included) can be placed between them.
+__device__ __forceinline__ void tmem_ld_x64_sync(uint32_t taddr, uint32_t (&r)[64]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -588,8 +596,9 @@ __device__ __forceinline__ void store_cols(const CUtensorMap* tmap_c, const Para
 
 // Epilogue warp e: lane quarter q = warp % 4, half h = e / 4.  Per tile it
 // drains chain 1 first (columns 256 + 64h .. +63, released before they are
-// stored), then chain 0 (columns 128h .. +127): at most 128 accumulator
-// words are live at a time.
+// stored), then chain 0 (columns 128h .. +127, 64 at a time, released after
+// the second load): at most 64 accumulator words are live at a time, so the
+// epilogue needs no spills.
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
                                               uint8_t* stage, uint32_t tmem_base, int q, int h, int lane) {
     const Sched S(p);
@@ -606,10 +615,8 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
             if (!warp_wait(&ss->acc_full[1], tc & 1u, ss, p.status)) break;
             tc_fence_after();
             uint32_t acc1[kChain1N / 2];
-            const uint32_t t1 = t_lane + (uint32_t)(kChain0N + (kChain1N / 2) * h);
-#pragma unroll
-            for (int c = 0; c < kChain1N / 64; ++c) tmem_ld_32x32b_x32(t1 + 32 * c, acc1 + 32 * c);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            static_assert(kChain1N / 2 == 64, "one 64-column load per warp");
+            tmem_ld_x64_sync(t_lane + (uint32_t)(kChain0N + (kChain1N / 2) * h), acc1);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ss->acc_empty[1]);
@@ -617,18 +624,28 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
                                      nb * BN + kChain0N + (kChain1N / 2) * h, y, rows_in);
         }
         {
+            // chain 0 in two 64-column halves: the first is stored before the
+            // second is loaded, so at most 64 accumulator words are live and
+            // none has to be spilled
             if (!warp_wait(&ss->acc_full[0], tc & 1u, ss, p.status)) break;
             tc_fence_after();
-            uint32_t acc0[kChain0N / 2];
+            constexpr int kHalf = kChain0N / 4;
+            static_assert(kHalf == 64, "one 64-column load per half");
             const uint32_t t0 = t_lane + (uint32_t)((kChain0N / 2) * h);
-#pragma unroll
-            for (int c = 0; c < kChain0N / 64; ++c) tmem_ld_32x32b_x32(t0 + 32 * c, acc0 + 32 * c);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ss->acc_empty[0]);
-            store_cols<kChain0N / 2>(tmap_c, p, acc0, alpha, stage, sw, lane, nb * BN + (kChain0N / 2) * h,
-                                     y, rows_in);
+            const int col0 = nb * BN + (kChain0N / 2) * h;
+            {
+                uint32_t acc0[kHalf];
+                tmem_ld_x64_sync(t0, acc0);
+                store_cols<kHalf>(tmap_c, p, acc0, alpha, stage, sw, lane, col0, y, rows_in);
+            }
+            {
+                uint32_t acc0[kHalf];
+                tmem_ld_x64_sync(t0 + kHalf, acc0);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ss->acc_empty[0]);
+                store_cols<kHalf>(tmap_c, p, acc0, alpha, stage, sw, lane, col0 + kHalf, y, rows_in);
+            }
         }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

@@ -145,3 +145,23 @@ def test_full_size_wgrad(nv):
     got = dw[:128].cpu().numpy()
     rel = np.linalg.norm(got - ref_rows) / np.linalg.norm(ref_rows)
     assert rel < 0.2
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_full_size_repeatable(nv, out_dtype):
+    # The accumulation order of every output element is fixed (K steps in
+    # order, one chain per element), so repeated launches on the same operands
+    # must agree bit for bit over the whole output, not only on the rows the
+    # oracle checks: a launch that read an accumulator or a scale slot at the
+    # wrong time shows up here as a difference.
+    x = workloads.activations(device="cuda")
+    w = workloads.weights(device="cuda")
+    qx, _ = nv.nvfp4_quantize(x)
+    qw, _ = nv.nvfp4_quantize(w, block="16x16")
+    first = nv.nvfp4_gemm(qx, qw, out_dtype=out_dtype)
+    for rep in range(6):
+        again = nv.nvfp4_gemm(qx, qw, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_sync_status() == nv.OK
+        diff = (again != first).nonzero()
+        assert diff.numel() == 0, f"launch {rep + 1} differs from the first at {diff.shape[0]} elements, first {diff[0].tolist()}"
