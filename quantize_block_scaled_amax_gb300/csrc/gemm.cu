@@ -36,11 +36,13 @@
 //               the scales come as long contiguous runs.
 //   warps 8-15  epilogue: two warps per lane quarter drain chain 1 (64
 //               columns each) and release it, store it, then drain chain 0
-//               (128 columns each) and release it; stores scale by alpha,
-//               convert and go through a 1 KB swizzled smem staging tile with
-//               TMA tensor stores.
-// Registers: 128 per thread (512 threads fill the register file); the
-// epilogue holds its 128 chain-0 accumulator words with a few words spilled.
+//               (128 columns each, 64 at a time, released after the second
+//               load); stores scale by alpha, convert and go through two 1 KB
+//               swizzled smem staging tiles per warp with TMA tensor stores.
+// Registers: at most 128 per thread (512 threads fill the register file).
+// The epilogue keeps at most 64 accumulator words live and takes each TMEM
+// load together with its wait, so nothing is spilled: a spill of registers
+// that a tcgen05.ld has not finished writing made repeated launches differ.
 // Every mbarrier wait is bounded: past the limit the waiter records
 // NVFP4_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag and all
 // roles drain out to the final barrier, where TMEM is freed.
@@ -79,7 +81,7 @@ constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
 constexpr int kStagingBytes = 32 * 32;     // one staging tile: 32 rows x 32 bytes
-constexpr int kStagingBufs = 2;            // per epilogue warp, used in turn
+constexpr int kStagingBufs = 2;            // per epilogue warp, filled as a pair
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;          // fp32 accumulator columns (chain 0: 0-255, chain 1: 256-383)
 constexpr uint32_t kSfaCols = kMmaPerStage * 4;         // 4 columns per MMA
