@@ -264,6 +264,9 @@ nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int
  *   C            device, [M][ldc] of out_dtype (bf16 or fp32), written whole.
  *   workspace    as nvfp4_quantize (may be NULL with 0 bytes: the GEMM
  *                needs none today).
+ * Deterministic: every output element accumulates its K steps in order in
+ * one FP32 accumulator, so the same operands give bit-identical C on every
+ * launch.
  */
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,
                         int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
