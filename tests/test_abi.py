@@ -156,3 +156,53 @@ def test_gemm_argument_checks_need_no_gpu(L):
     a = q.nvfp4_tensor(16, 16, 16, 128, 96, 48, 1, 0)     # K % 64 != 0
     b = q.nvfp4_tensor(16, 16, 16, 64, 96, 48, 1, 0)
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
+
+
+def test_rht_quantize_rowwise_argument_checks_need_no_gpu(L):
+    import quantize_block_scaled_amax_gb300 as q
+    t = q.nvfp4_tensor(16, 16, 16, 16, 64, 32, 1, 0)       # y [16][64], NVFP4
+    ws = 8192
+    args = lambda x, cols, rnd, out, wsb: L.nvfp4_rht_quantize_rowwise(x, 0, 16, cols, cols, rnd, 0, 0, out, 16,
+                                                                        wsb, None)
+    assert args(None, 64, 0, ctypes.byref(t), ws) == q.ERR_INVALID_ARG                 # null x
+    assert args(16, 40, 0, ctypes.byref(t), ws) == q.ERR_INVALID_ARG                   # cols % 16
+    assert args(16, 64, 5, ctypes.byref(t), ws) == q.ERR_INVALID_ARG                   # no such rounding
+    assert args(16, 64, 0, None, ws) == q.ERR_INVALID_ARG                              # no output
+    wrong = q.nvfp4_tensor(16, 16, 16, 32, 64, 32, 1, 0)    # [32][64] for a [16][64] input
+    assert args(16, 64, 0, ctypes.byref(wrong), ws) == q.ERR_INVALID_ARG
+    mx = q.nvfp4_tensor(16, 16, 16, 16, 48, 32, 1, 1)       # MXFP4 needs cols % 32
+    assert args(16, 48, 0, ctypes.byref(mx), ws) == q.ERR_INVALID_ARG
+    assert args(16, 64, 0, ctypes.byref(t), 64) == q.ERR_WORKSPACE                     # workspace too small
+    assert b"workspace" in L.nvfp4_last_error()
+
+
+def test_linear_argument_checks_need_no_gpu(L):
+    # the layer entry points check the context before their first call
+    import quantize_block_scaled_amax_gb300 as q
+    M, N, K = 64, 128, 64
+
+    def t(rows, cols, layout=1):
+        return q.nvfp4_tensor(16, 16, 16, rows, cols, max(16, cols // 2), layout, 0)
+
+    def ctx(**over):
+        c = q.nvfp4_linear_ctx(M, N, K, t(M, K), t(N, K), t(K, N), t(M, N), t(N, M), t(K, M), 16, 16384)
+        for k, v in over.items():
+            setattr(c, k, v)
+        return c
+
+    fwd = lambda c, x=16: L.nvfp4_linear_fwd(x, 16, 16, ctypes.byref(c) if c is not None else None, None)
+    assert fwd(None) == q.ERR_INVALID_ARG                                             # no context
+    assert fwd(ctx(), x=None) == q.ERR_INVALID_ARG                                    # null X
+    assert fwd(ctx(M=96)) == q.ERR_INVALID_ARG                                        # M % 64
+    assert fwd(ctx(xq=t(M, 2 * K))) == q.ERR_INVALID_ARG                              # xq shape
+    assert fwd(ctx(wq=t(N, K, layout=0))) == q.ERR_INVALID_ARG                        # wq needs MMA scales
+    assert fwd(ctx(wtq=t(N, K))) == q.ERR_INVALID_ARG                                 # wtq is [K][N]
+    assert b"wtq" in L.nvfp4_last_error()
+
+    bwd = lambda c, dw=16: L.nvfp4_linear_bwd(16, 16, 16, dw, 1, 2, ctypes.byref(c), None)
+    assert bwd(ctx(), dw=None) == q.ERR_INVALID_ARG                                   # null dW
+    assert bwd(ctx(K=0)) == q.ERR_INVALID_ARG                                         # empty
+    assert bwd(ctx(dyq=t(N, M))) == q.ERR_INVALID_ARG                                 # dyq is [M][N]
+    assert bwd(ctx(dytq=t(M, N))) == q.ERR_INVALID_ARG                                # dytq is [N][M]
+    assert bwd(ctx(xtq=t(K, M, layout=0))) == q.ERR_INVALID_ARG                       # xtq needs MMA scales
+    assert b"xtq" in L.nvfp4_last_error()
