@@ -66,7 +66,12 @@ typedef enum {
 } nvfp4_status;
 
 typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
-typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
+/* GEMM outputs: C = result in bf16 or FP32, or NVFP4_OUT_FP32_ADD: C is an
+ * FP32 matrix that the result is added into element by element (one
+ * correctly rounded FP32 add per element, C = fl(C + result)), as when a
+ * weight gradient is accumulated in FP32 over micro-batches (paper page,
+ * recipe paragraph: gradient accumulation stays in FP32). */
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1, NVFP4_OUT_FP32_ADD = 2 } nvfp4_out_dtype;
 typedef enum { NVFP4_BLOCK_1x16 = 0, NVFP4_BLOCK_16x16 = 1, NVFP4_BLOCK_MX1x32 = 2 } nvfp4_block;
 
 /*
@@ -130,7 +135,7 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout);
  * shape: the amax pass keeps one partial per CTA there (2048 at most, 8 KB);
  * nvfp4_quantize_with_rht keeps two sets (16 KB), which is what this
  * returns.  nvfp4_quantize, nvfp4_rht_quantize and nvfp4_rht_quantize_rowwise
- * need only the first 8 KB. */
+ * require only 8 KB (NVFP4_ERR_WORKSPACE below that). */
 size_t nvfp4_workspace_size(void);
 
 /*
@@ -151,9 +156,12 @@ size_t nvfp4_workspace_size(void);
  *   out_colwise  if non-NULL: describes x^T, [cols][rows], blocks along rows
  *                (rows % 16 == 0).  At least one output must be given; both
  *                get the same {A, S_dec, S_enc}.
- *   workspace    device, >= nvfp4_workspace_size() bytes, 16-byte aligned;
- *                no initial contents needed; must not be shared by calls
- *                that run concurrently.
+ *   workspace    device, >= 8 KB (half of nvfp4_workspace_size(); any
+ *                size from nvfp4_workspace_size() up is accepted), 16-byte
+ *                aligned; no initial contents needed.  The call writes it
+ *                and its second kernel reads it back, so two calls whose
+ *                work can overlap on the GPU (e.g. on unordered streams) must
+ *                not share one workspace.
  */
 nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
                             nvfp4_block block, nvfp4_round round, uint64_t seed,
@@ -173,9 +181,9 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_in_dtype dtype, int64_t rows, i
  *   allocates nothing; the caller still supplies x and the output buffers.
  *   Arguments, results and errors are those of nvfp4_quantize.
  *   Limit: the array holds 2048 partial maxima, which is what any call needs
- *   whatever the tensor size (the amax pass uses at most 2048 CTAs); a build
- *   whose workspace requirement exceeded the array would get
- *   NVFP4_ERR_WORKSPACE.
+ *   whatever the tensor size (the amax pass uses at most 2048 CTAs); the
+ *   library checks at compile time that the array covers nvfp4_quantize's
+ *   workspace requirement, so no tensor size is refused for lack of scratch.
  *   The first call on a device looks up the array's device address (and
  *   creates the CUDA context if needed); make that first call before any
  *   stream capture.  All calls on a device share the array and it keeps the
@@ -261,7 +269,9 @@ nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int
  *                NVFP4_SCALES_MMA scales (16-byte aligned buffers of
  *                nvfp4_scales_bytes() bytes), A->cols == B->cols == K,
  *                K % 64 == 0.
- *   C            device, [M][ldc] of out_dtype (bf16 or fp32), written whole.
+ *   C            device, [M][ldc] of out_dtype (bf16 or fp32), written whole;
+ *                with NVFP4_OUT_FP32_ADD an FP32 matrix the result is added
+ *                into (it must hold finite values or zeros beforehand).
  *   workspace    as nvfp4_quantize (may be NULL with 0 bytes: the GEMM
  *                needs none today).
  * Deterministic: every output element accumulates its K steps in order in
@@ -278,7 +288,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
  * paragraph: a few sensitive layers and the final ones stay in BF16).
  *   A            device bf16 [M][lda], B device bf16 [N][ldb] (both K-major,
  *                lda, ldb >= K and multiples of 8), K % 8 == 0.
- *   C            device, [M][ldc] of out_dtype, written whole.
+ *   C            device, [M][ldc] of out_dtype, written whole (or, with
+ *                NVFP4_OUT_FP32_ADD, added into).
  *   All pointers 16-byte aligned.  Errors as nvfp4_gemm.
  */
 nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
@@ -314,6 +325,9 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
  * for nvfp4_quantize_with_rht).  X, W, dY are bf16,
  * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
  * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).
+ * dw_accumulate = 0: dW = dY^T X (FP32, overwritten); nonzero: the Wgrad
+ * GEMM adds into dW (FP32 gradient accumulation across micro-batches, with
+ * the GEMM's NVFP4_OUT_FP32_ADD).
  */
 typedef struct {
     int64_t M, N, K;
@@ -325,6 +339,7 @@ typedef struct {
     nvfp4_tensor xtq;  /* [K][M]  */
     void* workspace;
     size_t workspace_bytes;
+    int32_t dw_accumulate;
 } nvfp4_linear_ctx;
 
 nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);

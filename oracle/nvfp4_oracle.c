@@ -20,6 +20,11 @@
  *
  * Parity status: every function below is pinned by a CPU test (see the test
  * files named oracle pins); Philox4x32-10 is pinned by known-answer vectors.
+ *
+ * Threads: loops over independent rows (or row blocks) carry an OpenMP
+ * pragma, so with -fopenmp they run on all host cores.  Each row's
+ * arithmetic is the same single-threaded code either way, and no value
+ * depends on which thread computed it.
  */
 #include <float.h>
 #include <math.h>
@@ -200,6 +205,7 @@ int nvfp4_oracle_rht_rows(float* x, int64_t rows, int64_t cols, uint64_t rht_see
     if (rows < 0 || cols < 0 || cols % 16) return ORACLE_ERR_INVALID;
     float d[16], y[16];
     nvfp4_oracle_rht16_signs(rht_seed, d);
+#pragma omp parallel for schedule(static) private(y)
     for (int64_t r = 0; r < rows; r++)
         for (int64_t c = 0; c < cols; c += 16) {
             nvfp4_oracle_rht16(x + r * cols + c, d, y);
@@ -213,11 +219,17 @@ int nvfp4_oracle_rht_rows(float* x, int64_t rows, int64_t cols, uint64_t rht_see
 /* A = max |x| over n values; non-finite input is an error. */
 int nvfp4_oracle_tensor_amax(const float* x, int64_t n, float* amax) {
     double a = 0.0;
+    int nonfinite = 0;
+#pragma omp parallel for schedule(static) reduction(max : a) reduction(| : nonfinite)
     for (int64_t i = 0; i < n; i++) {
-        if (!isfinite(x[i])) return ORACLE_ERR_NONFINITE;
+        if (!isfinite(x[i])) {
+            nonfinite = 1;
+            continue;
+        }
         double v = fabs((double)x[i]);
         if (v > a) a = v;
     }
+    if (nonfinite) return ORACLE_ERR_NONFINITE;
     *amax = (float)a; /* exact: a is one of the inputs */
     return ORACLE_OK;
 }
@@ -280,6 +292,7 @@ int nvfp4_oracle_quantize(const float* x, int64_t rows, int64_t cols, int64_t ro
     amax3[2] = s_enc;
 
     int64_t nkb = cols / 16;
+#pragma omp parallel for schedule(static)
     for (int64_t rb = 0; rb < rows; rb += block_h) {
         for (int64_t kb = 0; kb < nkb; kb++) {
             /* 2. block amax over the 1x16 or 16x16 block, then its E4M3 scale */
@@ -333,6 +346,7 @@ int nvfp4_oracle_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t
                             int block_h, float s_dec, double* out) {
     if (rows < 0 || cols % 16 || (block_h != 1 && block_h != 16)) return ORACLE_ERR_INVALID;
     int64_t nkb = cols / 16;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; r++)
         for (int64_t c = 0; c < cols; c++) {
             uint32_t byte = codes[r * (cols / 2) + c / 2];
@@ -384,6 +398,7 @@ int nvfp4_oracle_mx_quantize(const float* x, int64_t rows, int64_t cols, int64_t
     for (int64_t i = 0; i < rows * cols; i++)
         if (!isfinite(x[i])) return ORACLE_ERR_NONFINITE;
     int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; r++) {
         for (int64_t b = 0; b < nb; b++) {
             float bamax = 0.0f;
@@ -419,6 +434,7 @@ int nvfp4_oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int6
                                double* out) {
     if (rows < 0 || cols % 32) return ORACLE_ERR_INVALID;
     int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; r++)
         for (int64_t c = 0; c < cols; c++) {
             uint32_t byte = codes[r * (cols / 2) + c / 2];

@@ -28,7 +28,7 @@ __all__ = [
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA = range(7)
 IN_BF16, IN_FP32 = 0, 1
-OUT_BF16, OUT_FP32 = 0, 1
+OUT_BF16, OUT_FP32, OUT_FP32_ADD = 0, 1, 2
 BLOCK_1x16, BLOCK_16x16, BLOCK_MX1x32 = 0, 1, 2
 FORMAT_NVFP4, FORMAT_MXFP4 = 0, 1
 RTN, SR = 0, 1
@@ -56,7 +56,8 @@ class nvfp4_linear_ctx(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("xq", nvfp4_tensor), ("wq", nvfp4_tensor), ("wtq", nvfp4_tensor), ("dyq", nvfp4_tensor),
                 ("dytq", nvfp4_tensor), ("xtq", nvfp4_tensor),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("dw_accumulate", ctypes.c_int32)]
 
 
 _lib = None
@@ -135,15 +136,23 @@ def nvfp4_workspace_size() -> int:
 
 
 _ws: dict = {}
+_ws_lock = threading.Lock()
 
 
-def _workspace(device) -> torch.Tensor:
-    key = (device.index if device.index is not None else torch.cuda.current_device())
-    w = _ws.get(key)
-    if w is None:
-        w = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
-        _ws[key] = w
-    return w
+def _workspace(device, stream_handle: int) -> torch.Tensor:
+    """The amax-partials workspace of the quantize wrappers, one per
+    (device, stream).  A quantize call writes its workspace in its first
+    kernel and reads it back in the next, so two calls whose work can overlap
+    on the GPU must not share one: calls on one stream run in order, calls on
+    different streams get different buffers.  Each buffer lives as long as
+    the process (16 KB per stream used)."""
+    key = (device.index if device.index is not None else torch.cuda.current_device(), int(stream_handle))
+    with _ws_lock:
+        w = _ws.get(key)
+        if w is None:
+            w = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
+            _ws[key] = w
+        return w
 
 
 class QTensor:
@@ -208,10 +217,11 @@ def nvfp4_quantize(x: torch.Tensor, block: str = "1x16", round: str = "rtn", see
         out_colwise = empty_qtensor(cols, rows, x.device, scale_layout, fmt)
     r = out_rowwise.c() if rowwise else None
     c = out_colwise.c() if colwise else None
-    ws = _workspace(x.device)
+    sh = _stream(stream)
+    ws = _workspace(x.device, sh)
     st = lib().nvfp4_quantize(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _BLOCKS[block], _ROUNDS[round],
                               seed, ctypes.byref(r) if r is not None else None,
-                              ctypes.byref(c) if c is not None else None, ws.data_ptr(), ws.numel(), _stream(stream))
+                              ctypes.byref(c) if c is not None else None, ws.data_ptr(), ws.numel(), sh)
     _check(st, "nvfp4_quantize")
     return (out_rowwise if rowwise else None), (out_colwise if colwise else None)
 
@@ -249,9 +259,10 @@ def nvfp4_rht_quantize(x: torch.Tensor, round: str = "rtn", seed: int = 0, rht_s
     if out_colwise is None:
         out_colwise = empty_qtensor(cols, rows, x.device, scale_layout, fmt)
     c = out_colwise.c()
-    ws = _workspace(x.device)
+    sh = _stream(stream)
+    ws = _workspace(x.device, sh)
     st = lib().nvfp4_rht_quantize(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
-                                  rht_seed, ctypes.byref(c), ws.data_ptr(), ws.numel(), _stream(stream))
+                                  rht_seed, ctypes.byref(c), ws.data_ptr(), ws.numel(), sh)
     _check(st, "nvfp4_rht_quantize")
     return out_colwise
 
@@ -270,10 +281,10 @@ def nvfp4_quantize_with_rht(x: torch.Tensor, round: str = "rtn", seed: int = 0, 
     if out_colwise is None:
         out_colwise = empty_qtensor(cols, rows, x.device, scale_layout)
     r, c = out_rowwise.c(), out_colwise.c()
-    ws = _workspace(x.device)
+    sh = _stream(stream)
+    ws = _workspace(x.device, sh)
     st = lib().nvfp4_quantize_with_rht(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
-                                       rht_seed, ctypes.byref(r), ctypes.byref(c), ws.data_ptr(), ws.numel(),
-                                       _stream(stream))
+                                       rht_seed, ctypes.byref(r), ctypes.byref(c), ws.data_ptr(), ws.numel(), sh)
     _check(st, "nvfp4_quantize_with_rht")
     return out_rowwise, out_colwise
 
@@ -288,19 +299,31 @@ def nvfp4_rht_quantize_rowwise(x: torch.Tensor, round: str = "rtn", seed: int = 
     if out_rowwise is None:
         out_rowwise = empty_qtensor(rows, cols, x.device, scale_layout, fmt)
     r = out_rowwise.c()
-    ws = _workspace(x.device)
+    sh = _stream(stream)
+    ws = _workspace(x.device, sh)
     st = lib().nvfp4_rht_quantize_rowwise(x.data_ptr(), _in_dtype(x), rows, cols, x.stride(0), _ROUNDS[round], seed,
-                                          rht_seed, ctypes.byref(r), ws.data_ptr(), ws.numel(), _stream(stream))
+                                          rht_seed, ctypes.byref(r), ws.data_ptr(), ws.numel(), sh)
     _check(st, "nvfp4_rht_quantize_rowwise")
     return out_rowwise
 
 
+def _out_mode(out: torch.Tensor, accumulate: bool) -> int:
+    if accumulate:
+        if out.dtype != torch.float32:
+            raise ValueError("accumulate=True needs an FP32 output to add into")
+        return OUT_FP32_ADD
+    return {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32}[out.dtype]
+
+
 def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
-               stream=None) -> torch.Tensor:
-    """C[M][N] = dequant(a) @ dequant(b)^T on the FP4 tensor cores (FP32 accumulation)."""
+               stream=None, accumulate: bool = False) -> torch.Tensor:
+    """C[M][N] = dequant(a) @ dequant(b)^T on the FP4 tensor cores (FP32
+    accumulation); accumulate=True adds the result into the FP32 ``out``."""
     if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an existing FP32 output")
         out = torch.empty(a.rows, b.rows, dtype=out_dtype, device=a.codes.device)
-    od = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32}[out.dtype]
+    od = _out_mode(out, accumulate)
     ca, cb = a.c(), b.c()
     st = lib().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), out.data_ptr(), od, out.stride(0), None, 0,
                           _stream(stream))
@@ -309,16 +332,19 @@ def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tens
 
 
 def nvfp4_gemm_bf16(a: torch.Tensor, b: torch.Tensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
-                    stream=None) -> torch.Tensor:
-    """C[M][N] = a @ b^T for bf16 a [M][K], b [N][K] on the tensor cores (FP32 accumulation)."""
+                    stream=None, accumulate: bool = False) -> torch.Tensor:
+    """C[M][N] = a @ b^T for bf16 a [M][K], b [N][K] on the tensor cores (FP32
+    accumulation); accumulate=True adds the result into the FP32 ``out``."""
     for t in (a, b):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
             raise ValueError("a and b must be 2D row-major bf16 CUDA tensors")
     if a.shape[1] != b.shape[1]:
         raise ValueError(f"K mismatch: {tuple(a.shape)} vs {tuple(b.shape)}")
     if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an existing FP32 output")
         out = torch.empty(a.shape[0], b.shape[0], dtype=out_dtype, device=a.device)
-    od = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32}[out.dtype]
+    od = _out_mode(out, accumulate)
     st = lib().nvfp4_gemm_bf16(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), out.data_ptr(), od,
                                out.stride(0), a.shape[0], b.shape[0], a.shape[1], _stream(stream))
     _check(st, "nvfp4_gemm_bf16")
@@ -352,9 +378,10 @@ class LinearContext:
         self.xtq = empty_qtensor(K, M, device)
         self.workspace = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
 
-    def c(self) -> nvfp4_linear_ctx:
+    def c(self, dw_accumulate: bool = False) -> nvfp4_linear_ctx:
         return nvfp4_linear_ctx(self.M, self.N, self.K, self.xq.c(), self.wq.c(), self.wtq.c(), self.dyq.c(),
-                                self.dytq.c(), self.xtq.c(), self.workspace.data_ptr(), self.workspace.numel())
+                                self.dytq.c(), self.xtq.c(), self.workspace.data_ptr(), self.workspace.numel(),
+                                1 if dw_accumulate else 0)
 
 
 def nvfp4_linear_fwd(X: torch.Tensor, W: torch.Tensor, ctx: LinearContext, Y: torch.Tensor | None = None,
@@ -371,16 +398,21 @@ def nvfp4_linear_fwd(X: torch.Tensor, W: torch.Tensor, ctx: LinearContext, Y: to
 
 
 def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor, ctx: LinearContext, sr_seed: int, rht_seed: int,
-                     dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None):
+                     dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None,
+                     accumulate_dw: bool = False):
+    """Dgrad and Wgrad of the layer; with accumulate_dw=True the FP32 Wgrad
+    result is added into the given dW instead of overwriting it."""
     if dX is None:
         dX = torch.empty(ctx.M, ctx.K, dtype=torch.bfloat16, device=dY.device)
     if dW is None:
+        if accumulate_dw:
+            raise ValueError("accumulate_dw=True needs an existing FP32 dW")
         dW = torch.empty(ctx.N, ctx.K, dtype=torch.float32, device=dY.device)
     for t, shape, dt in ((dY, (ctx.M, ctx.N), torch.bfloat16), (X, (ctx.M, ctx.K), torch.bfloat16),
                          (dX, (ctx.M, ctx.K), torch.bfloat16), (dW, (ctx.N, ctx.K), torch.float32)):
         if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
             raise ValueError(f"expected contiguous {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
-    c = ctx.c()
+    c = ctx.c(dw_accumulate=accumulate_dw)
     _check(lib().nvfp4_linear_bwd(dY.data_ptr(), X.data_ptr(), dX.data_ptr(), dW.data_ptr(), sr_seed, rht_seed,
                                   ctypes.byref(c), _stream(stream)), "nvfp4_linear_bwd")
     return dX, dW

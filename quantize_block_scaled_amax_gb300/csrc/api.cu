@@ -127,8 +127,8 @@ nvfp4_status check_input(const void* x, nvfp4_in_dtype dtype, int64_t rows, int6
 }
 
 nvfp4_status check_workspace(void* ws, size_t bytes) {
-    if (!ws || bytes < (size_t)kMaxPartials * sizeof(uint32_t))
-        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", (size_t)kMaxPartials * 4, bytes);
+    if (!ws || bytes < kSinglePassWorkspaceBytes)
+        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", kSinglePassWorkspaceBytes, bytes);
     if (!aligned16(ws)) return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     return NVFP4_OK;
 }
@@ -173,7 +173,7 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout) {
     return scales_bytes(rows, cols, scale_layout);
 }
 
-size_t nvfp4_workspace_size(void) { return 2 * (size_t)kMaxPartials * sizeof(uint32_t); }
+size_t nvfp4_workspace_size(void) { return 2 * kSinglePassWorkspaceBytes; }
 
 const char* nvfp4_last_error(void) { return g_err; }
 
@@ -309,8 +309,8 @@ nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_
         return st;
     if (out_rowwise->format != NVFP4_FORMAT_NVFP4 || out_colwise->format != NVFP4_FORMAT_NVFP4)
         return fail(NVFP4_ERR_INVALID_ARG, "outputs must have format NVFP4 (MXFP4 has no amax pass to share)");
-    if (!workspace || workspace_bytes < 2 * (size_t)kMaxPartials * sizeof(uint32_t))
-        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", 2 * (size_t)kMaxPartials * 4,
+    if (!workspace || workspace_bytes < 2 * kSinglePassWorkspaceBytes)
+        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", 2 * kSinglePassWorkspaceBytes,
                     workspace_bytes);
     if (!aligned16(workspace)) return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     DeviceInfo* dev;
@@ -391,9 +391,9 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     if (!aligned16(A->scales) || !aligned16(B->scales))
         return fail(NVFP4_ERR_INVALID_ARG, "GEMM scale buffers must be 16-byte aligned");
     if (A->format != B->format) return fail(NVFP4_ERR_INVALID_ARG, "GEMM operands must share one format");
-    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32 && out_dtype != NVFP4_OUT_FP32_ADD)
         return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
-    const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    const int esz = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     if (ldc < B->rows || (ldc * esz) % 16 || !aligned16(C))
         return fail(NVFP4_ERR_INVALID_ARG, "C: ldc must be >= N and 16-byte rows, C 16-byte aligned");
     DeviceInfo* dev;
@@ -412,7 +412,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     g.M = A->rows;
     g.N = B->rows;
     g.K = A->cols;
-    g.out_fp32 = out_dtype == NVFP4_OUT_FP32;
+    g.out_fp32 = out_dtype != NVFP4_OUT_BF16;
+    g.accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
     g.mx = A->format == NVFP4_FORMAT_MXFP4;
     g.status = dev->status;
     g.num_sms = dev->num_sms;
@@ -432,9 +433,9 @@ nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t 
     if (K % 8) return fail(NVFP4_ERR_INVALID_ARG, "K %lld not a multiple of 8", (long long)K);
     if (lda < K || ldb < K || lda % 8 || ldb % 8)
         return fail(NVFP4_ERR_INVALID_ARG, "lda, ldb must be >= K and multiples of 8 elements");
-    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32 && out_dtype != NVFP4_OUT_FP32_ADD)
         return fail(NVFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
-    const int esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    const int esz = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     if (ldc < N || (ldc * esz) % 16) return fail(NVFP4_ERR_INVALID_ARG, "ldc must be >= N with 16-byte rows");
     if (!aligned16(A) || !aligned16(B) || !aligned16(C))
         return fail(NVFP4_ERR_INVALID_ARG, "A, B, C must be 16-byte aligned");
@@ -451,7 +452,8 @@ nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t 
     g.M = M;
     g.N = N;
     g.K = K;
-    g.out_fp32 = out_dtype == NVFP4_OUT_FP32;
+    g.out_fp32 = out_dtype != NVFP4_OUT_BF16;
+    g.accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
     g.status = dev->status;
     g.num_sms = dev->num_sms;
     const char* msg = nullptr;
@@ -529,7 +531,8 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
     if ((st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
                                  ctx->workspace_bytes, stream)))
         return st;
-    return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, NVFP4_OUT_FP32, K, nullptr, 0, stream);
+    return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, ctx->dw_accumulate ? NVFP4_OUT_FP32_ADD : NVFP4_OUT_FP32, K, nullptr,
+                      0, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -545,6 +548,9 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
 // in it has to start at zero: each call's amax pass writes every slot that
 // the same call's encode pass reads.
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kMaxPartials];
+// nvfp4_quantize's workspace check is what the array must satisfy.
+static_assert(sizeof(g_noalloc_scratch) >= kSinglePassWorkspaceBytes,
+              "the fixed scratch array must hold one amax pass's partials");
 
 namespace nvfp4 {
 namespace {
@@ -579,12 +585,8 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t
                                     const nvfp4_tensor* out_rowwise, const nvfp4_tensor* out_colwise,
                                     nvfp4_stream_t stream) {
     g_err[0] = 0;
-    // nvfp4_quantize keeps one partial per amax CTA (kMaxPartials at most);
-    // refuse if the fixed array were ever smaller than that.
-    const size_t need = (size_t)kMaxPartials * sizeof(uint32_t);
-    if (need > sizeof(g_noalloc_scratch))
-        return fail(NVFP4_ERR_WORKSPACE, "quantize needs %zu bytes of scratch, the fixed array holds %zu", need,
-                    sizeof(g_noalloc_scratch));
+    // the array covers nvfp4_quantize's workspace requirement for any shape
+    // (checked at compile time above), so no size can exceed it
     void* scratch = nullptr;
     nvfp4_status st = noalloc_scratch(&scratch);
     if (st) return st;

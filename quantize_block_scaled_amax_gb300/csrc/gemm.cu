@@ -258,6 +258,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                  : "memory");
 }
 
+// The same tile added element-wise into global memory (FP32 adds, done by
+// the memory system): C += tile, for accumulating into an FP32 gradient.
+__device__ __forceinline__ void tma_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -312,6 +321,7 @@ struct Params {
     int n_katoms;             // atoms per 128-row group: 4 * ceil(K / 256)
     int b_groups;             // 128-row groups of B: ceil(N / 128)
     int out_fp32;
+    int accumulate;           // FP32 output added into C instead of stored
     int mx;                   // MXFP4 operands (UE8M0 scales, 32-element blocks)
     int bf16;                 // BF16 operands: no scales, 64 K elements per stage, alpha = 1
     uint32_t* status;
@@ -589,7 +599,10 @@ __device__ __forceinline__ void store_cols(const CUtensorMap* tmap_c, const Para
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const int x = col0 + per * (c2 + b);
-                if (rows_in && x < p.N) tma_store_2d(tmap_c, stage + b * kStagingBytes, x, y);
+                if (rows_in && x < p.N) {
+                    if (p.accumulate) tma_add_2d(tmap_c, stage + b * kStagingBytes, x, y);
+                    else tma_store_2d(tmap_c, stage + b * kStagingBytes, x, y);
+                }
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
@@ -818,6 +831,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.n_katoms = 4 * p.num_k;
     p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
+    p.accumulate = g.accumulate;
     p.mx = g.mx;
     p.bf16 = 0;
     p.status = g.status;
@@ -869,6 +883,7 @@ int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
     p.num_n = (int)((g.N + BN - 1) / BN);
     p.num_k = (int)((g.K + 63) / 64);
     p.out_fp32 = g.out_fp32;
+    p.accumulate = g.accumulate;
     p.bf16 = 1;
     p.status = g.status;
     const int64_t tiles = (int64_t)p.num_m * p.num_n;

@@ -14,6 +14,9 @@ constexpr int kQuantThreads = 256;
 constexpr int kColThreads = 128;
 constexpr int k2dThreads = 256;
 constexpr int kMaxPartials = 2048;  // workspace holds one uint32 partial max per amax CTA
+// Workspace bytes of one amax pass (what nvfp4_quantize, nvfp4_rht_quantize and
+// nvfp4_rht_quantize_rowwise require); nvfp4_quantize_with_rht keeps two sets.
+constexpr size_t kSinglePassWorkspaceBytes = (size_t)kMaxPartials * sizeof(uint32_t);
 
 struct ScaleOut;
 
@@ -55,6 +58,7 @@ struct GemmArgs {
     int64_t ldc;  // elements
     int64_t M, N, K;
     int out_fp32;
+    int accumulate;  // fp32 only: C += result (TMA reduce-add) instead of C = result
     int mx;  // MXFP4 operands: UE8M0 scales per 32 elements, scale_vec::2X
     uint32_t* status;
     int num_sms;
@@ -71,6 +75,7 @@ struct GemmBf16Args {
     int64_t lda, ldb, ldc;  // elements
     int64_t M, N, K;
     int out_fp32;
+    int accumulate;  // fp32 only: C += result
     uint32_t* status;
     int num_sms;
 };

@@ -15,6 +15,14 @@ rounding decisions, and a run started from the same ``seed_base`` repeats
 them exactly.  The RHT sign vector uses ``rht_seed`` (one per layer; both
 Wgrad operands of a call share it, as the transform requires).
 
+FP32 gradient accumulation: the recipe keeps gradient accumulation in FP32
+(paper page, recipe paragraph).  With ``main_grad=True`` a layer adds each
+backward's FP32 Wgrad result into ``weight.main_grad`` (an FP32 tensor of
+the weight's shape, zeros when first created; the optimizer reads it and
+zeroes it between steps) inside the Wgrad GEMM itself, and leaves
+``weight.grad`` unset; otherwise ``weight.grad`` gets the Wgrad result cast
+to the weight's dtype.
+
 Precision: the paper page keeps some linear layers in BF16 (the last blocks
 of the network) and switches the whole model to BF16 for the final part of
 training to close the remaining loss gap.  A layer's ``precision`` is
@@ -84,10 +92,11 @@ class NVFP4LinearFunction(torch.autograd.Function):
 
     Returns Y [..., N] bf16.  Gradients: dX bf16, dW in W's dtype (the Wgrad
     GEMM accumulates and writes FP32; the cast to bf16 is the one rounding
-    this wrapper adds)."""
+    this wrapper adds), or, when ``main_grad`` (an FP32 [N, K] tensor) is
+    given, no dW: the Wgrad GEMM adds its FP32 result into ``main_grad``."""
 
     @staticmethod
-    def forward(ctx, x, w, contexts: _Contexts, seeds: _SeedCounter, rht_seed: int):
+    def forward(ctx, x, w, contexts: _Contexts, seeds: _SeedCounter, rht_seed: int, main_grad=None):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
         w = w.contiguous()
@@ -102,6 +111,7 @@ class NVFP4LinearFunction(torch.autograd.Function):
         ctx.seeds = seeds
         ctx.rht_seed = rht_seed
         ctx.w_dtype = w.dtype
+        ctx.main_grad = main_grad
         return y.reshape(*lead, n)
 
     @staticmethod
@@ -109,11 +119,15 @@ class NVFP4LinearFunction(torch.autograd.Function):
         (x2,) = ctx.saved_tensors
         lc = ctx.lc
         dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
-        dx, dw = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed)
         # linear_fwd quantized W into lc.wtq, which Dgrad reads; a later forward
         # through the same context must not run before this backward is done,
         # which the stream order guarantees for single-stream training.
-        return dx.reshape(*ctx.lead, lc.K), dw.to(ctx.w_dtype), None, None, None
+        if ctx.main_grad is not None:
+            dx, _ = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed,
+                                     dW=ctx.main_grad, accumulate_dw=True)
+            return dx.reshape(*ctx.lead, lc.K), None, None, None, None, None
+        dx, dw = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed)
+        return dx.reshape(*ctx.lead, lc.K), dw.to(ctx.w_dtype), None, None, None, None
 
 
 class BF16LinearFunction(torch.autograd.Function):
@@ -122,7 +136,7 @@ class BF16LinearFunction(torch.autograd.Function):
     bf16; Y, dX and dW are bf16.  M, N, K must be multiples of 8."""
 
     @staticmethod
-    def forward(ctx, x, w):
+    def forward(ctx, x, w, main_grad=None):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
         w = w.contiguous()
@@ -135,6 +149,7 @@ class BF16LinearFunction(torch.autograd.Function):
         y = nvfp4_gemm_bf16(x2, w)                          # [M][N] = X W^T
         ctx.save_for_backward(x2, w)
         ctx.lead = lead
+        ctx.main_grad = main_grad
         return y.reshape(*lead, w.shape[0])
 
     @staticmethod
@@ -142,8 +157,11 @@ class BF16LinearFunction(torch.autograd.Function):
         x2, w = ctx.saved_tensors
         dy2 = dy.reshape(-1, w.shape[0]).to(torch.bfloat16).contiguous()
         dx = nvfp4_gemm_bf16(dy2, nvfp4_transpose_bf16(w))  # [M][K] = dY W
+        if ctx.main_grad is not None:                      # main_grad += dY^T X, FP32
+            nvfp4_gemm_bf16(nvfp4_transpose_bf16(dy2), nvfp4_transpose_bf16(x2), out=ctx.main_grad, accumulate=True)
+            return dx.reshape(*ctx.lead, w.shape[1]), None, None
         dw = nvfp4_gemm_bf16(nvfp4_transpose_bf16(dy2), nvfp4_transpose_bf16(x2))  # [N][K] = dY^T X
-        return dx.reshape(*ctx.lead, w.shape[1]), dw
+        return dx.reshape(*ctx.lead, w.shape[1]), dw, None
 
 
 class NVFP4Linear(torch.nn.Module):
@@ -151,10 +169,11 @@ class NVFP4Linear(torch.nn.Module):
     tensor cores.  ``weight`` is a bf16 parameter [out_features, in_features]
     (the high-precision master copy stays with the optimizer, as in the
     recipe); in_features, out_features and the token count must be multiples
-    of 64."""
+    of 64.  ``main_grad=True``: the Wgrad result is accumulated in FP32 into
+    ``weight.main_grad`` instead of being returned as ``weight.grad``."""
 
     def __init__(self, in_features: int, out_features: int, device=None, seed_base: int = 1, rht_seed: int = 2,
-                 precision: str = "nvfp4"):
+                 precision: str = "nvfp4", main_grad: bool = False):
         super().__init__()
         if in_features % 64 or out_features % 64:
             raise ValueError("in_features and out_features must be multiples of 64")
@@ -166,14 +185,26 @@ class NVFP4Linear(torch.nn.Module):
         self._contexts = _Contexts()
         self._seeds = _SeedCounter(seed_base)
         self.rht_seed = int(rht_seed)
+        self.use_main_grad = bool(main_grad)
+
+    def _main_grad(self):
+        if not self.use_main_grad:
+            return None
+        g = getattr(self.weight, "main_grad", None)
+        if g is None or g.shape != self.weight.shape or g.device != self.weight.device:
+            g = torch.zeros(self.weight.shape, dtype=torch.float32, device=self.weight.device)
+            self.weight.main_grad = g
+        return g
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         if self.precision == "bf16":
-            return BF16LinearFunction.apply(x, self.weight)
-        return NVFP4LinearFunction.apply(x, self.weight, self._contexts, self._seeds, self.rht_seed)
+            return BF16LinearFunction.apply(x, self.weight, self._main_grad())
+        return NVFP4LinearFunction.apply(x, self.weight, self._contexts, self._seeds, self.rht_seed,
+                                         self._main_grad())
 
     def extra_repr(self) -> str:
-        return f"in_features={self.weight.shape[1]}, out_features={self.weight.shape[0]}, precision={self.precision}"
+        return (f"in_features={self.weight.shape[1]}, out_features={self.weight.shape[0]}, precision={self.precision}, "
+                f"main_grad={self.use_main_grad}")
 
 
 def set_precision(module: torch.nn.Module, precision: str) -> int:

@@ -38,11 +38,28 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
-def test_struct_layout_matches_header(L):
+def test_struct_layout_matches_header(L, tmp_path):
+    # the binding's ctypes structures against the C compiler's view of the
+    # header: every field's offset and each struct's size
+    import subprocess
     import quantize_block_scaled_amax_gb300 as q
-    # nvfp4_tensor: 3 pointers, 3 int64, 2 int32 = 56 bytes on LP64
-    assert ctypes.sizeof(q.nvfp4_tensor) == 56
-    assert ctypes.sizeof(q.nvfp4_linear_ctx) == 3 * 8 + 6 * 56 + 8 + 8
+    structs = {"nvfp4_tensor": q.nvfp4_tensor, "nvfp4_linear_ctx": q.nvfp4_linear_ctx}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "nvfp4.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} sizeof %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for name, cls in structs.items():
+        assert got[(name, "sizeof")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)
 
 
 def test_status_strings(L):

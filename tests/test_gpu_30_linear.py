@@ -44,6 +44,13 @@ def test_linear_fwd_bwd(nv, mnk):
     assert_gemm_close(y.float().cpu().numpy(), d["xq"] @ d["wq"].T, d["xq"], d["wq"], bf16=True, what="Y")
     assert_gemm_close(dx.float().cpu().numpy(), d["dyq"] @ d["wtq"].T, d["dyq"], d["wtq"], bf16=True, what="dX")
     assert_gemm_close(dw.cpu().numpy(), d["dytq"] @ d["xtq"].T, d["dytq"], d["xtq"], bf16=False, what="dW")
+    # FP32-output twins of the layer's bf16 Fprop and Dgrad, on the same
+    # quantized operands: the strict relative-Frobenius bound
+    y32 = nv.nvfp4_gemm(ctx.xq, ctx.wq, out_dtype=torch.float32)
+    dx32 = nv.nvfp4_gemm(ctx.dyq, ctx.wtq, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_gemm_close(y32.cpu().numpy(), d["xq"] @ d["wq"].T, d["xq"], d["wq"], bf16=False, what="Y fp32")
+    assert_gemm_close(dx32.cpu().numpy(), d["dyq"] @ d["wtq"].T, d["dyq"], d["wtq"], bf16=False, what="dX fp32")
     # fidelity to the unquantized layer (a loose sanity bound, not parity)
     yr = xn.astype(np.float64) @ wn.astype(np.float64).T
     assert np.linalg.norm(y.float().cpu().numpy() - yr) / np.linalg.norm(yr) < 0.2

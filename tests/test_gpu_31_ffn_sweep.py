@@ -31,7 +31,8 @@ def _row(q, r):
     return oracle.dequantize(q)[r - q["row0"]]
 
 
-@pytest.mark.parametrize("m, which", [(2048, "up"), (2048, "down"), (8192, "down"), (32768, "up")])
+@pytest.mark.parametrize("m, which", [(2048, "up"), (2048, "down"), (8192, "up"), (8192, "down"), (32768, "up"),
+                                      (32768, "down")])
 def test_ffn_linear_sampled(nv, m, which):
     n, k = (D_FFN, D_MODEL) if which == "up" else (D_MODEL, D_FFN)
     sr, rh = workloads.SR_SEED, workloads.RHT_SEED
@@ -84,3 +85,17 @@ def test_ffn_linear_sampled(nv, m, which):
     a = np.stack([_row(odyt[r], r) for r in rn])
     b = np.stack([_row(oxt[r], r) for r in rk])
     assert_gemm_close(dw[rn][:, rk].cpu().numpy(), a @ b.T, a, b, bf16=False, what=f"{which} M={m} dW")
+
+    # FP32-output twins of Fprop and Dgrad on the same quantized operands
+    # (the layer returns bf16 Y and dX): the strict relative-Frobenius bound
+    # over the sampled entries
+    y32 = nv.nvfp4_gemm(ctx.xq, ctx.wq, out_dtype=torch.float32)
+    dx32 = nv.nvfp4_gemm(ctx.dyq, ctx.wtq, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    a = np.stack([_row(ox[r], r) for r in rm])
+    b = np.stack([_row(ow[r], r) for r in rn])
+    assert_gemm_close(y32[rm][:, rn].cpu().numpy(), a @ b.T, a, b, bf16=False, what=f"{which} M={m} Y fp32")
+    a = np.stack([_row(ody[r], r) for r in rm])
+    b = np.stack([_row(owt[r], r) for r in rk])
+    assert_gemm_close(dx32[rm][:, rk].cpu().numpy(), a @ b.T, a, b, bf16=False, what=f"{which} M={m} dX fp32")
