@@ -346,6 +346,15 @@ nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linea
 nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,
                               uint64_t rht_seed, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
 
+/* Bound, in nanoseconds, of every wait inside the GEMM kernels (a pipeline
+ * stage that never fills, a barrier that never completes): past it the
+ * kernel records NVFP4_ERR_TIMEOUT in the status word, lets its MMAs and
+ * copies in flight finish, and returns, so the context stays usable.  0
+ * restores the default (4 s).  Applies to GEMMs launched after the call, in
+ * every thread; returns the previous setting.  Meant for tests and
+ * diagnostics: a bound far below a GEMM's running time aborts it. */
+uint64_t nvfp4_set_wait_limit_ns(uint64_t limit_ns);
+
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NVFP4_ERR_NONFINITE, NVFP4_ERR_TIMEOUT or NVFP4_OK
  * (NVFP4_ERR_CUDA if the synchronization itself failed). */

@@ -22,7 +22,7 @@ __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
     "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
     "nvfp4_transpose_bf16",
-    "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_set_wait_limit_ns", "nvfp4_scales_bytes", "nvfp4_workspace_size",
     "empty_qtensor", "scales_as_linear",
 ]
 
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_linear_fwd.argtypes = [vp, vp, vp, ctypes.POINTER(nvfp4_linear_ctx), vp]
             L.nvfp4_linear_bwd.restype = st
             L.nvfp4_linear_bwd.argtypes = [vp, vp, vp, vp, u64, u64, ctypes.POINTER(nvfp4_linear_ctx), vp]
+            L.nvfp4_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.nvfp4_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.nvfp4_sync_status.restype = st
             L.nvfp4_sync_status.argtypes = [vp]
             L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -416,6 +418,12 @@ def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor, ctx: LinearContext, sr_s
     _check(lib().nvfp4_linear_bwd(dY.data_ptr(), X.data_ptr(), dX.data_ptr(), dW.data_ptr(), sr_seed, rht_seed,
                                   ctypes.byref(c), _stream(stream)), "nvfp4_linear_bwd")
     return dX, dW
+
+
+def nvfp4_set_wait_limit_ns(limit_ns: int) -> int:
+    """Bound of every device-side wait in the GEMM kernels (0: the default,
+    4 s); returns the previous setting.  For tests and diagnostics."""
+    return int(lib().nvfp4_set_wait_limit_ns(int(limit_ns)))
 
 
 def nvfp4_sync_status(stream=None) -> int:

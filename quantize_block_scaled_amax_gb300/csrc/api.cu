@@ -1,6 +1,7 @@
 // C ABI of the NVFP4 engine: argument checks on the host, then kernel
 // launches on the caller's stream.  See include/nvfp4.h for the contract.
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -18,6 +19,9 @@ static __device__ uint32_t g_status_word;
 namespace {
 
 thread_local char g_err[512];
+
+// Bound of every device-side wait of the GEMM (0: the kernel's default, 4 s).
+std::atomic<uint64_t> g_wait_limit_ns{0};
 
 nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
     va_list ap;
@@ -415,6 +419,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     g.out_fp32 = out_dtype != NVFP4_OUT_BF16;
     g.accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
     g.mx = A->format == NVFP4_FORMAT_MXFP4;
+    g.timeout_ns = g_wait_limit_ns.load();
     g.status = dev->status;
     g.num_sms = dev->num_sms;
     const char* msg = nullptr;
@@ -454,6 +459,7 @@ nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t 
     g.K = K;
     g.out_fp32 = out_dtype != NVFP4_OUT_BF16;
     g.accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
+    g.timeout_ns = g_wait_limit_ns.load();
     g.status = dev->status;
     g.num_sms = dev->num_sms;
     const char* msg = nullptr;
@@ -593,6 +599,8 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, nvfp4_in_dtype dtype, int64_t
     return nvfp4_quantize(x, dtype, rows, cols, ldx, block, round, seed, out_rowwise, out_colwise, scratch,
                           sizeof(g_noalloc_scratch), stream);
 }
+
+uint64_t nvfp4_set_wait_limit_ns(uint64_t limit_ns) { return g_wait_limit_ns.exchange(limit_ns); }
 
 nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream) {
     g_err[0] = 0;

@@ -60,6 +60,7 @@ struct GemmArgs {
     int out_fp32;
     int accumulate;  // fp32 only: C += result (TMA reduce-add) instead of C = result
     int mx;  // MXFP4 operands: UE8M0 scales per 32 elements, scale_vec::2X
+    uint64_t timeout_ns;  // bound of each device-side wait (0: the default, 4 s)
     uint32_t* status;
     int num_sms;
 };
@@ -76,6 +77,7 @@ struct GemmBf16Args {
     int64_t M, N, K;
     int out_fp32;
     int accumulate;  // fp32 only: C += result
+    uint64_t timeout_ns;  // bound of each device-side wait (0: the default, 4 s)
     uint32_t* status;
     int num_sms;
 };
