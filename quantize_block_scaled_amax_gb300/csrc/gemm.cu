@@ -46,10 +46,9 @@
 // on a completed phase), one lane waits for each warp, the MMA issuer waits
 // once per stage, and the copies of a stage are split between two threads.
 //   warps 8-15  epilogue: two warps per lane quarter, 128 columns each; each
-//               drains 64 columns, stages them through a 4 KB smem box and
-//               stores them by TMA, drains the other 64, releases the
-//               accumulator to the MMA issuer and stores the rest, so the next
-//               tile's MMAs wait only for the two TMEM loads.
+//               stores its first 64 columns by TMA through a 4 KB smem box,
+//               loads the rest, releases the accumulator to the MMA issuer,
+//               and stores the rest while the next tile's MMAs run.
 // TMEM scale-factor placement (measured with a probe MMA whose scale bytes
 // encode their own TMEM address): in both the 1-SM and the pair form, A row
 // r of an SM is read from lane r, column base + r / 32; B row n (all N rows,
@@ -395,6 +394,20 @@ __device__ __forceinline__ void tmem_ld_x64_sync(uint32_t taddr, uint32_t (&r)[6
         : "memory");
 }
 
+// 32 accumulator columns of the warp's 32 lanes, returned once loaded.
+__device__ __forceinline__ void tmem_ld_x32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -408,6 +421,7 @@ struct Params {
     const float* b_amax;
     int M, N, K;
     int num_m, num_n, num_k;  // pair tiles along M and N, stages along K
+    int group_m;              // M tiles per band of the tile raster
     int n_katoms;             // atoms per 128-row group: 4 * ceil(K / 256)
     int a_groups, b_groups;   // 128-row groups of A and B: ceil(rows / 128)
     int out_fp32;
@@ -418,8 +432,13 @@ struct Params {
     uint32_t* status;
 };
 
-// Tile schedule: cluster c takes pair tiles c, c + clusters, ... with M
-// fastest, so neighbouring clusters share their B tile in L2.
+// Tile schedule: cluster c takes pair tiles c, c + clusters, ... of a
+// banded raster.  The M tiles are cut into bands of `group_m` rows; a band's
+// tiles come one after the other, M fastest, so the clusters running at one
+// time share a few B panels and the band's A panels, which stay in L2 while
+// the band's B panels stream past them once.  (With one band over a long-K
+// operand, say 32 A panels of 3 MB, the A panels fell out of L2 between
+// waves and were read from DRAM six times over.)
 struct Sched {
     int num_tiles, cid, nclusters;
     __device__ explicit Sched(const Params& p) {
@@ -430,8 +449,13 @@ struct Sched {
     __device__ int count() const { return cid < num_tiles ? (num_tiles - cid + nclusters - 1) / nclusters : 0; }
     __device__ void tile(int i, const Params& p, int& mt, int& nt) const {
         const int t = cid + i * nclusters;
-        nt = t / p.num_m;
-        mt = t - nt * p.num_m;
+        const int band_tiles = p.group_m * p.num_n;
+        const int band = t / band_tiles;
+        const int m0 = band * p.group_m;
+        const int rows = min(p.group_m, p.num_m - m0);  // the last band may be shorter
+        const int r = t - band * band_tiles;
+        nt = r / rows;
+        mt = m0 + (r - nt * rows);
     }
 };
 
@@ -516,13 +540,12 @@ __device__ __forceinline__ bool mma_loop(const Params& p, SharedState* ss, uint8
     // start-address field, MMA j adds 32 j >> 4
     const uint64_t adesc0 = smem_desc(smem_u32(stages));
     const uint64_t bdesc0 = smem_desc(smem_u32(stages + kATileBytes));
-    uint32_t it = 0;
+    int s = 0;            // ring stage of the next MMAs, and its phase parity
+    uint32_t ph = 0;
     for (int i = 0; i < S.count(); ++i) {
         if (!mbar_wait(&ss->acc_empty, ((uint32_t)i & 1u) ^ 1u, ss, p.status, p.timeout_ns)) return false;
         tc_fence_after();
-        for (int kt = 0; kt < p.num_k; ++kt, ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1u;
+        for (int kt = 0; kt < p.num_k; ++kt) {
             if (!mbar_wait(&ss->full[s], ph, ss, p.status, p.timeout_ns)) return false;
             tc_fence_after();
             const uint64_t soff = (uint64_t)((uint32_t)(s * kStageBytes) >> 4);
@@ -540,6 +563,10 @@ __device__ __forceinline__ bool mma_loop(const Params& p, SharedState* ss, uint8
                     mma_nvf4(tmem_base, adesc, bdesc, idesc, sf + 4 * j, sf + kSfaCols + 8 * j, acc);
             }
             mma_commit_pair(&ss->empty[s]);
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         mma_commit_pair(&ss->acc_full);
     }
@@ -659,51 +686,35 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tmap_c, const Param
     }
 }
 
-// Writes 64 accumulator columns of the warp's 32 rows (alpha applied) into
-// the staging box and stores them at column x: bf16, one 32 x 128-byte box;
-// fp32, two boxes of 32 columns one after the other.  Row r's 16-byte chunk
-// c sits at chunk position c ^ (r % 8) (the 128-byte swizzle).  The caller
-// has made sure the buffer is free.
-__device__ __forceinline__ void stage_and_store(const CUtensorMap* tmap_c, const Params& p, const uint32_t (&acc)[64],
-                                                float alpha, uint8_t* staging, int lane, int x, int y, bool rows_in) {
-    const int sw = lane & 7;
+// Staging writes of one 32-row box (128 bytes per row, the C tensor map's
+// 128-byte swizzle: row r's 16-byte chunk c at chunk position c ^ (r % 8)).
+// bf16: 64 columns given as 32 packed words; fp32: 32 columns, scaled here.
+__device__ __forceinline__ void stage_bf16(const uint32_t* w, uint8_t* staging, int lane) {
     uint8_t* row = staging + lane * BKB;
-    if (!p.out_fp32) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t* a = acc + 8 * c;
-            const uint4 v = make_uint4(
-                pack_bf16x2(__fmul_rn(__uint_as_float(a[0]), alpha), __fmul_rn(__uint_as_float(a[1]), alpha)),
-                pack_bf16x2(__fmul_rn(__uint_as_float(a[2]), alpha), __fmul_rn(__uint_as_float(a[3]), alpha)),
-                pack_bf16x2(__fmul_rn(__uint_as_float(a[4]), alpha), __fmul_rn(__uint_as_float(a[5]), alpha)),
-                pack_bf16x2(__fmul_rn(__uint_as_float(a[6]), alpha), __fmul_rn(__uint_as_float(a[7]), alpha)));
-            *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = v;
-        }
-        store_box(tmap_c, p, staging, lane, x, y, rows_in);
-        return;
-    }
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                                                                               w[4 * c + 3]);
+}
+
+__device__ __forceinline__ void stage_f32(const uint32_t* a, float alpha, uint8_t* staging, int lane) {
+    uint8_t* row = staging + lane * BKB;
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-        if (b == 1) staging_free(lane);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t* a = acc + 32 * b + 4 * c;
-            const uint4 v = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[0]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(a[1]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(a[2]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(a[3]), alpha)));
-            *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = v;
-        }
-        store_box(tmap_c, p, staging, lane, x + 32 * b, y, rows_in);
-    }
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(a[4 * c]), alpha)),
+                       __float_as_uint(__fmul_rn(__uint_as_float(a[4 * c + 1]), alpha)),
+                       __float_as_uint(__fmul_rn(__uint_as_float(a[4 * c + 2]), alpha)),
+                       __float_as_uint(__fmul_rn(__uint_as_float(a[4 * c + 3]), alpha)));
 }
 
 // Epilogue warp (both CTAs): lane quarter q (its TMEM lanes 32q..32q+31, the
 // CTA's rows 32q..), column half h (columns 128h..128h+127 of the tile).
-// The first 64 columns are stored before the second 64 are loaded, and the
-// accumulator is released right after that second load: at most 64
-// accumulator words are live per thread, nothing is spilled, and the next
-// tile's MMAs start while the stores drain.
+// The first 64 columns are loaded, staged and handed to TMA (the staging
+// buffer is free: the previous tile's stores have long finished reading
+// it), then the last 64 are loaded and the accumulator is released at once;
+// their conversion, staging and stores overlap the next tile's MMAs.  At
+// most 64 accumulator words are live per thread, so nothing is spilled.
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
                                               uint8_t* staging, uint32_t tmem_base, int q, int h, int lane,
                                               uint32_t rank) {
@@ -711,6 +722,14 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
     const float alpha = p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
     const uint32_t t_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
     const uint32_t acc_empty_l = leader_addr(&ss->acc_empty);
+    auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (rank == 0) mbar_arrive_local(&ss->acc_empty);
+            else mbar_arrive_leader(acc_empty_l);
+        }
+    };
     for (int i = 0; i < S.count(); ++i) {
         int mt, nt;
         S.tile(i, p, mt, nt);
@@ -719,23 +738,53 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
         const int y = mt * kPairM + (int)rank * BM + 32 * q;
         const bool rows_in = y < p.M;
         const int x0 = nt * BN + 128 * h;
-        {
-            uint32_t acc[64];
-            tmem_ld_x64_sync(t_lane, acc);
-            staging_free(lane);
-            stage_and_store(tmap_c, p, acc, alpha, staging, lane, x0, y, rows_in);
-        }
-        {
-            uint32_t acc[64];
-            tmem_ld_x64_sync(t_lane + 64, acc);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (rank == 0) mbar_arrive_local(&ss->acc_empty);
-                else mbar_arrive_leader(acc_empty_l);
+        if (!p.out_fp32) {
+            // columns 0-63 packed to bf16 and written to staging, 64-127
+            // loaded, then the release; the stores follow
+            uint32_t a[64];
+            tmem_ld_x64_sync(t_lane, a);
+            {
+                uint32_t w[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    w[k] = pack_bf16x2(__fmul_rn(__uint_as_float(a[2 * k]), alpha),
+                                       __fmul_rn(__uint_as_float(a[2 * k + 1]), alpha));
+                staging_free(lane);
+                stage_bf16(w, staging, lane);
             }
+            tmem_ld_x64_sync(t_lane + 64, a);
+            release();
+            store_box(tmap_c, p, staging, lane, x0, y, rows_in);
+            {
+                uint32_t w[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    w[k] = pack_bf16x2(__fmul_rn(__uint_as_float(a[2 * k]), alpha),
+                                       __fmul_rn(__uint_as_float(a[2 * k + 1]), alpha));
+                staging_free(lane);
+                stage_bf16(w, staging, lane);
+            }
+            store_box(tmap_c, p, staging, lane, x0 + 64, y, rows_in);
+        } else {
+            // columns 0-63 staged and stored, 64-127 loaded, then the release
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                uint32_t a[32];
+                tmem_ld_x32_sync(t_lane + 32 * b, a);
+                staging_free(lane);
+                stage_f32(a, alpha, staging, lane);
+                store_box(tmap_c, p, staging, lane, x0 + 32 * b, y, rows_in);
+            }
+            uint32_t a2[32], a3[32];
+            tmem_ld_x32_sync(t_lane + 64, a2);
+            tmem_ld_x32_sync(t_lane + 96, a3);
+            release();
             staging_free(lane);
-            stage_and_store(tmap_c, p, acc, alpha, staging, lane, x0 + 64, y, rows_in);
+            stage_f32(a2, alpha, staging, lane);
+            store_box(tmap_c, p, staging, lane, x0 + 64, y, rows_in);
+            staging_free(lane);
+            stage_f32(a3, alpha, staging, lane);
+            store_box(tmap_c, p, staging, lane, x0 + 96, y, rows_in);
         }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -925,6 +974,21 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
     return (int)cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel, ta, tb, tcm, p);
 }
 
+// M tiles per band of the raster (see Sched): as many as keep the band's A
+// panels (panel_bytes each: kPairM rows of codes and scales over the whole K)
+// within kL2BandBytes, then evened out over the bands.
+#ifndef NVFP4_GEMM_L2_BAND_MB
+#define NVFP4_GEMM_L2_BAND_MB 32
+#endif
+constexpr double kL2BandBytes = (double)NVFP4_GEMM_L2_BAND_MB * 1048576.0;
+
+int band_rows(int num_m, double panel_bytes) {
+    int gmax = (int)(kL2BandBytes / panel_bytes);
+    if (gmax < 1) gmax = 1;
+    const int bands = (num_m + gmax - 1) / gmax;
+    return (num_m + bands - 1) / bands;
+}
+
 int make_c_map(CUtensorMap* tcm, const void* c, int64_t M, int64_t N, int64_t ldc, bool fp32, const char** msg) {
     if (fp32) return make_map(tcm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, M, N, ldc * 4, 32, 32, msg);
     return make_map(tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, M, N, ldc * 2, 64, 32, msg);
@@ -956,6 +1020,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.num_n = (int)((g.N + BN - 1) / BN);
     p.num_k = (int)((g.K + BK - 1) / BK);
     p.n_katoms = 4 * p.num_k;
+    p.group_m = band_rows(p.num_m, (double)kPairM * ((double)g.K / 2 + (double)g.K / 16));
     p.a_groups = (int)((g.M + 127) / 128);
     p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
@@ -986,6 +1051,7 @@ int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
     p.num_m = (int)((g.M + kPairM - 1) / kPairM);
     p.num_n = (int)((g.N + BN - 1) / BN);
     p.num_k = (int)((g.K + 63) / 64);
+    p.group_m = band_rows(p.num_m, (double)kPairM * 2.0 * (double)g.K);
     p.a_groups = (int)((g.M + 127) / 128);
     p.b_groups = (int)((g.N + 127) / 128);
     p.out_fp32 = g.out_fp32;
