@@ -208,6 +208,8 @@ def gpu_bench(args):
 
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
            for _ in range(args.steps)]
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
     if rank == 0:
         sampler.start()
@@ -217,10 +219,12 @@ def gpu_bench(args):
     torch.cuda.synchronize()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                  # evict L2 between steps (not timed)
+        step_evs[s][0].record(stream)
         for (name, fn), (e0, e1) in zip(ops, evs[s]):
             e0.record(stream)
             fn()
             e1.record(stream)
+        step_evs[s][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -232,6 +236,9 @@ def gpu_bench(args):
             per_op[name] += e0.elapsed_time(e1)
     total_ms = max_over_ranks(sum(per_op.values()), dev)
     ms_per_step = total_ms / args.steps
+    # one event pair around each whole step as well: the per-op sum leaves out
+    # any idle time between the launches the host issues one by one
+    step_wall_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_evs), dev) / args.steps
     value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd/bwd.
@@ -309,6 +316,7 @@ def gpu_bench(args):
     rht_rows = None if args.no_mx else rht_rows_measure(nv, x, w, dy, flush, stream, max(5, args.steps // 10))
     bf16_gemm = None if args.no_mx else bf16_gemm_measure(nv, x, w, flush, stream, max(5, args.steps // 10),
                                                           _peaks())
+    ffn = None if args.no_ffn else ffn_measure(nv, flush, stream, max(5, args.steps // 4), _peaks())
 
     if rank != 0:
         if world > 1:
@@ -317,7 +325,9 @@ def gpu_bench(args):
         return None
 
     peaks = _peaks()
-    fp4_peak = peaks["bf16_sustained"] * FP4_OVER_BF16
+    # each GEMM is event-timed on its own, a fraction of a millisecond: the
+    # burst figure applies
+    fp4_peak = peaks["bf16"] * FP4_OVER_BF16
     kernels = {}
     for name, ms in per_op.items():
         avg = ms / args.steps
@@ -338,7 +348,7 @@ def gpu_bench(args):
                  "frac": round(gemm_ach / fp4_peak, 4),
                  "traffic": _profile_traffic("gemm.cu", "gemm_nvf4_fprop_8192x20480x5120.txt"),
                  "kernel": "nvf4_gemm_kernel (avg of Fprop, Dgrad, Wgrad launches)",
-                 "peak_source": f"{peaks['source']} sustained bf16 {peaks['bf16_sustained']} TFLOP/s x "
+                 "peak_source": f"{peaks['source']} burst bf16 {peaks['bf16']} TFLOP/s x "
                                 f"{FP4_OVER_BF16:g} (nominal FP4/BF16 ratio)"}
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                   "frac": round(quant_gbs / peaks["hbm"], 4), "traffic": None,
@@ -348,6 +358,7 @@ def gpu_bench(args):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step_wall": round(step_wall_ms, 4),
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate; fp32 quantize)",
         "data": "synthetic (seeded: X N(0,1)+0.1% x50 outliers, W N(0,0.02), dY Student-t(3)*1e-3)",
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "l2": "flushed between steps (256 MB write)",
@@ -363,6 +374,7 @@ def gpu_bench(args):
         "mxfp4": mx,
         "rht_fprop_dgrad_quantize": rht_rows,
         "bf16_fallback_gemm": bf16_gemm,
+        "ffn": ffn,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -412,36 +424,86 @@ def _oracle_sample_desc(m, n):
             f"value = 3*2*{m}*{n}*{K} FLOP / oracle time")
 
 
+def _host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
 def cpu_baseline_subprocess(m: int, n: int):
-    """Time the oracle in a fresh single-threaded process (no fork after CUDA)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--cpu-sample-m", str(m),
-                        "--cpu-sample-n", str(n)], capture_output=True, text=True, env=env, timeout=1800)
-    if r.returncode != 0:
-        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    """Time the oracle in fresh processes (none forked after CUDA): on all
+    host cores over the full step (every quantization in full, the GEMMs on
+    sampled output rows, extrapolated), and on one core over a slice."""
+    out = {}
+    for mode, threads in (("full", _host_cores()), ("slice", 1)):
+        env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+                   MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", mode, "--cpu-sample-m",
+                            str(m), "--cpu-sample-n", str(n)], capture_output=True, text=True, env=env, timeout=1800)
+        if r.returncode != 0:
+            out[mode] = {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+        else:
+            out[mode] = json.loads(r.stdout.strip().splitlines()[-1])
+    res = dict(out["full"])
+    res["single_core"] = out["slice"]
+    return res
 
 
-def _single_thread():
-    # must run before numpy / torch load their thread pools
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = "1"
+def _timed(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return r, time.perf_counter() - t0
 
 
-def cpu_baseline_only(m: int, n: int):
+def cpu_baseline_only(mode: str, m: int, n: int):
     import torch
-    torch.set_num_threads(1)
+    threads = int(os.environ.get("OMP_NUM_THREADS", "1"))
+    torch.set_num_threads(threads)
     import oracle
     oracle.build()
     oracle_step(*oracle_inputs(16, 64, K))          # load and warm the library
-    inputs = oracle_inputs(m, n, K)
-    t0 = time.perf_counter()
-    oracle_step(*inputs)
-    dt = time.perf_counter() - t0
-    flops = 3 * 2.0 * m * n * K
-    print(json.dumps({"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                      "seconds": round(dt, 3), "sample": _oracle_sample_desc(m, n)}))
+    if mode == "slice":
+        inputs = oracle_inputs(m, n, K)
+        _, dt = _timed(lambda: oracle_step(*inputs))
+        flops = 3 * 2.0 * m * n * K
+        print(json.dumps({"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                          "seconds": round(dt, 3), "sample": _oracle_sample_desc(m, n)}))
+        return
+    # full: the oracle on the whole layer step, every quantization in full;
+    # each GEMM's dequantized B operand in full and 256 sampled output rows,
+    # its row time extrapolated linearly to all rows
+    import numpy as np
+    import workloads
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    x = workloads.activations(M, K).float().numpy()
+    w = workloads.weights(N, K).float().numpy()
+    dy = workloads.gradients(M, N).float().numpy()
+    t_quant = 0.0
+    q = {}
+    for name, fn in (("x", lambda: oracle.quantize(x)),
+                     ("w", lambda: oracle.quantize(w, block="16x16")),
+                     ("wt", lambda: oracle.quantize(w, layout="col", block="16x16")),
+                     ("dy", lambda: oracle.quantize(dy, rounding="sr", seed=sr)),
+                     ("dyt", lambda: oracle.quantize(dy, layout="col", rounding="sr", seed=sr, rht_seed=rh)),
+                     ("xt", lambda: oracle.quantize(x, layout="col", rht_seed=rh))):
+        q[name], dt = _timed(fn)
+        t_quant += dt
+    rows = 256
+    t_gemm_est = 0.0
+    for a, b in (("x", "w"), ("dy", "wt"), ("dyt", "xt")):
+        bd, t_b = _timed(lambda: oracle.dequantize(q[b]))
+        qa = dict(q[a], codes=q[a]["codes"][:rows], scales=q[a]["scales"][:rows])
+        _, t_rows = _timed(lambda: oracle.dequantize(qa) @ bd.T)
+        t_gemm_est += t_b + t_rows * q[a]["codes"].shape[0] / rows
+        del bd
+    est = t_quant + t_gemm_est
+    flops = 3 * 2.0 * M * N * K
+    print(json.dumps({
+        "value": round(flops / est / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+        "seconds": round(est, 3), "seconds_quantize_measured": round(t_quant, 3),
+        "seconds_gemm_extrapolated": round(t_gemm_est, 3),
+        "sample": (f"oracle on the full layer step M={M} N={N} K={K}: all six quantizations of the recipe in full "
+                   f"(measured); the three FP64 GEMMs on {rows} sampled output rows each plus the dequantized B "
+                   f"operand, row time extrapolated linearly to all rows; value = 3*2*M*N*K FLOP / "
+                   f"(quantize time + extrapolated GEMM time); OpenMP threads over rows = cores")}))
 
 
 def reference_arm(args):
@@ -449,7 +511,8 @@ def reference_arm(args):
     if rank != 0:
         return None
     import torch
-    torch.set_num_threads(1)
+    cores = _host_cores()                      # the oracle's OpenMP rows and numpy's matmul use every core
+    torch.set_num_threads(cores)
     import oracle
     oracle.build()
     m, n = args.ref_sample_m, args.ref_sample_n
@@ -467,7 +530,7 @@ def reference_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle: FP32 steps emulated in FP64, FP64 GEMM)",
         "data": "synthetic", "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
                                         "sample": _oracle_sample_desc(m, n)},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": _oracle_sample_desc(m, n)},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -538,6 +601,77 @@ def bf16_gemm_measure(nv, x, w, flush, stream, steps, peaks):
             "frac": round(tf / peaks["bf16"], 4), "peak_source": f"{peaks['source']} cuBLAS bf16 burst"}
 
 
+def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
+    """The FFN block of the 12B model (up 5120 -> 20480, down 20480 -> 5120,
+    no nonlinearity between them), forward and backward, at each token count:
+    per step 6 GEMMs (Fprop, Dgrad, Wgrad of both linears) and the
+    quantizations of the recipe, op by op through the C ABI as the main step.
+    The down linear's input is the up linear's output and the up linear's
+    output gradient is the down linear's input gradient.  Not part of `value`."""
+    import torch
+    import workloads
+    from quantize_block_scaled_amax_gb300 import LinearContext
+    d_model, d_ffn = workloads.D_MODEL, workloads.D_FFN
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    fp4_peak = peaks["bf16"] * FP4_OVER_BF16
+    out = {}
+    for m in ms:
+        dev = flush.device
+        x = workloads.activations(m, d_model, outliers=False, seed=workloads.SEED_BASE + 20, device=dev)
+        w1 = workloads.weights(d_ffn, d_model, seed=workloads.SEED_BASE + 21, device=dev)
+        w2 = workloads.weights(d_model, d_ffn, seed=workloads.SEED_BASE + 22, device=dev)
+        dy2 = workloads.gradients(m, d_model, seed=workloads.SEED_BASE + 23, device=dev)
+        c1, c2 = LinearContext(m, d_ffn, d_model, dev), LinearContext(m, d_model, d_ffn, dev)
+        y1 = torch.empty(m, d_ffn, dtype=torch.bfloat16, device=dev)
+        y2 = torch.empty(m, d_model, dtype=torch.bfloat16, device=dev)
+        dy1 = torch.empty(m, d_ffn, dtype=torch.bfloat16, device=dev)      # = dX of the down linear
+        dx = torch.empty(m, d_model, dtype=torch.bfloat16, device=dev)
+        dw1 = torch.empty(d_ffn, d_model, dtype=torch.float32, device=dev)
+        dw2 = torch.empty(d_model, d_ffn, dtype=torch.float32, device=dev)
+
+        def lin(tag, c, xin, w, y):
+            return [(f"{tag}_quant_x", lambda: nv.nvfp4_quantize(xin, out_rowwise=c.xq)),
+                    (f"{tag}_quant_w", lambda: nv.nvfp4_quantize(w, block="16x16", colwise=True, out_rowwise=c.wq,
+                                                                 out_colwise=c.wtq)),
+                    (f"{tag}_gemm_fprop", lambda: nv.nvfp4_gemm(c.xq, c.wq, out=y))]
+
+        def lin_bwd(tag, c, dyin, xin, dxo, dwo):
+            return [(f"{tag}_quant_dy", lambda: nv.nvfp4_quantize_with_rht(dyin, round="sr", seed=sr, rht_seed=rh,
+                                                                           out_rowwise=c.dyq, out_colwise=c.dytq)),
+                    (f"{tag}_gemm_dgrad", lambda: nv.nvfp4_gemm(c.dyq, c.wtq, out=dxo)),
+                    (f"{tag}_rht_quant_x", lambda: nv.nvfp4_rht_quantize(xin, round="rtn", rht_seed=rh,
+                                                                         out_colwise=c.xtq)),
+                    (f"{tag}_gemm_wgrad", lambda: nv.nvfp4_gemm(c.dytq, c.xtq, out=dwo))]
+
+        ops = (lin("up", c1, x, w1, y1) + lin("down", c2, y1, w2, y2) + lin_bwd("down", c2, dy2, y1, dy1, dw2)
+               + lin_bwd("up", c1, dy1, x, dx, dw1))
+        nsteps = max(3, steps if m <= 8192 else steps // 2)
+        per = _time_ops(nv, ops, flush, stream, nsteps)
+        step_ms = sum(per.values()) / nsteps
+        flops = 6 * 2.0 * m * d_model * d_ffn
+        gemm_ms = sum(v for k, v in per.items() if "gemm" in k) / nsteps
+        quant_ms = step_ms - gemm_ms
+        # algorithmic bytes of the quantize ops: amax read + encode read + codes and scales per layout
+        bx, bh = m * d_model, m * d_ffn
+        qbytes = (2 * 2 * bx + bx * 9 // 16) + (2 * 2 * bh + bh * 9 // 16)            # quant_x of up, down
+        qbytes += 2 * (2 * 2 * d_model * d_ffn + 2 * d_model * d_ffn * 9 // 16)       # both W, 16x16 both layouts
+        qbytes += (3 * 2 * bx + 2 * bx * 9 // 16) + (3 * 2 * bh + 2 * bh * 9 // 16)   # dY of down, up (rowwise + RHT)
+        qbytes += (2 * 2 * bh + bh * 9 // 16) + (2 * 2 * bx + bx * 9 // 16)           # RHT X^T of down, up
+        gemm_tf = 6 * 2.0 * m * d_model * d_ffn / (gemm_ms * 1e-3) / 1e12
+        quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
+        out[str(m)] = {"ms_per_step": round(step_ms, 4), "tflops": round(flops / (step_ms * 1e-3) / 1e12, 1),
+                       "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tf, 1),
+                       "gemm_frac": round(gemm_tf / fp4_peak, 4), "quant_ms": round(quant_ms, 4),
+                       "quant_gbs": round(quant_gbs, 1), "quant_frac": round(quant_gbs / peaks["hbm"], 4),
+                       "steps": nsteps, "gpu_launches_per_step": 24,
+                       "ops_ms": {k: round(v / nsteps, 4) for k, v in per.items()}}
+        del x, w1, w2, dy2, c1, c2, y1, y2, dy1, dx, dw1, dw2, ops
+        torch.cuda.empty_cache()
+    return {"workload": "FFN block fwd+bwd of the 12B model (up 5120->20480, down 20480->5120), bf16 inputs, "
+                        "6 NVFP4 GEMMs + the recipe's quantizations per step", "by_tokens": out,
+            "peak_source": f"GEMM: {peaks['source']} burst bf16 x {FP4_OVER_BF16:g}; quantize: HBM copy"}
+
+
 def mx_measure(nv, x, w, dy, flush, stream, steps):
     """The same layer step with MXFP4 operands (32-element blocks, UE8M0
     scales, no tensor scale: one read per quantize; weights 1x32 in both
@@ -604,7 +738,8 @@ def profile_case(args):
         del x, w
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        # "gemm_fp32": FP32 output, as the Wgrad GEMM writes it
+        y = torch.empty(m, n, dtype=torch.float32 if op.endswith("fp32") else torch.bfloat16, device=dev)
         torch.cuda.synchronize()
         nv.nvfp4_gemm(qx, qw, out=y)
     elif op == "quant_x_rtn":
@@ -642,7 +777,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mx", action="store_true",
                     help="skip the MXFP4 comparison step and the RHT-on-Fprop/Dgrad quantize timings")
-    ap.add_argument("--cpu-baseline-only", action="store_true")
+    ap.add_argument("--no-ffn", action="store_true", help="skip the FFN block (up+down, M sweep) measurement")
+    ap.add_argument("--cpu-baseline-only", default=None, choices=["full", "slice"])
     ap.add_argument("--cpu-sample-m", type=int, default=512)
     ap.add_argument("--cpu-sample-n", type=int, default=4096)
     ap.add_argument("--profile", default=None,
@@ -650,15 +786,13 @@ def main():
     ap.add_argument("--m", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)
     ap.add_argument("--k", type=int, default=0)
-    ap.add_argument("--ref-sample-m", type=int, default=64)
-    ap.add_argument("--ref-sample-n", type=int, default=256)
+    ap.add_argument("--ref-sample-m", type=int, default=256)
+    ap.add_argument("--ref-sample-n", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.cpu_baseline_only or args.impl == "reference":
-        _single_thread()
     if args.cpu_baseline_only:
-        cpu_baseline_only(args.cpu_sample_m, args.cpu_sample_n)
+        cpu_baseline_only(args.cpu_baseline_only, args.cpu_sample_m, args.cpu_sample_n)
         return
     if args.profile:
         profile_case(args)
