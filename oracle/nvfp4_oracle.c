@@ -158,15 +158,24 @@ void nvfp4_oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], ui
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Random word of element i of a logical tensor for stochastic rounding:
- * key = seed, counter = (i/4 low, i/4 high, stream 0, 0), word i mod 4. */
+/* Random word of element i of a logical tensor for stochastic rounding.
+ * One Philox4x32-10 block (key = seed, counter = (i/8 low, i/8 high, 0, 0))
+ * gives the 16-bit random values of eight consecutive elements: element i
+ * takes half (i mod 8) of the block read as eight 16-bit halves, low half of
+ * each word first, i.e. half (i mod 2) of word (i mod 8)/2.  It is returned
+ * in the top 16 bits of the word (the low 16 bits zero), so the encode's
+ * decision "up iff u * 2^-24 < frac" with u = word >> 8 reads it as
+ * h * 2^-16 < frac: P(up) = ceil(frac * 2^16) / 2^16, within 2^-16 of the
+ * fractional distance the blog's technique list asks for. */
 uint32_t nvfp4_oracle_sr_bits(uint64_t seed, uint64_t i) {
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
-    uint64_t q = i >> 2;
+    uint64_t q = i >> 3;
     uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), 0u, 0u};
     uint32_t out[4];
     nvfp4_oracle_philox4x32_10(ctr, key, out);
-    return out[i & 3u];
+    uint32_t word = out[(i & 7u) >> 1];
+    uint32_t half = (i & 1u) ? (word >> 16) : (word & 0xFFFFu);
+    return half << 16;
 }
 
 /* ---- 16-point random Hadamard transform -------------------------------- */

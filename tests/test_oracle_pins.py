@@ -138,12 +138,17 @@ def test_philox_known_answer_vectors():
 
 
 def test_sr_bits_counter_mapping():
-    # element i uses word i%4 of the block with counter (i//4 low, i//4 high, 0, 0)
-    kat0 = [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
-    assert [oracle.sr_bits(0, i) for i in range(4)] == kat0
-    i = (1 << 34) + 6
-    w = oracle.philox4x32_10([(i >> 2) & 0xFFFFFFFF, i >> 34, 0, 0], [7, 0])
-    assert oracle.sr_bits(7, i) == w[2]
+    # elements 8j..8j+7 share the block with counter (j low, j high, 0, 0);
+    # element i takes 16-bit half i%8 of it (low half of each word first),
+    # returned in the top half of the word
+    kat0 = [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]    # seed 0, counter 0
+    halves = [0xE8D5, 0x6627, 0xC58D, 0xE169, 0xAC4C, 0xBC57, 0xDBD8, 0x9B00]
+    assert [oracle.sr_bits(0, i) for i in range(8)] == [h << 16 for h in halves]
+    assert [oracle.sr_bits(0, i) >> 16 for i in range(8)] == [
+        (kat0[k >> 1] >> (16 * (k & 1))) & 0xFFFF for k in range(8)]
+    i = (1 << 35) + 13
+    w = oracle.philox4x32_10([(i >> 3) & 0xFFFFFFFF, i >> 35, 0, 0], [7, 0])
+    assert oracle.sr_bits(7, i) == (w[2] >> 16) << 16
 
 
 # ---- tensor and block scales ----------------------------------------------
@@ -294,7 +299,8 @@ def test_sr_unbiased_over_a_million_draws(v):
     assert abs(err) <= 4 * sigma + 1e-12
     # empirical probability of rounding up
     p_up = np.mean(np.abs(deq) == hi)
-    assert abs(p_up - frac) <= 4 * np.sqrt(frac * (1 - frac) / n) + 2.0 ** -24
+    # (16-bit random values: P(up) = ceil(frac * 2^16) / 2^16)
+    assert abs(p_up - frac) <= 4 * np.sqrt(frac * (1 - frac) / n) + 2.0 ** -16
 
 
 def test_sr_extreme_random_words():
