@@ -192,10 +192,12 @@ __device__ __forceinline__ uint64_t x2_fma_rp(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
-// E2M1 stochastic rounding of one value v with its 32-bit random word w, as
-// the grid value it rounds to (sign kept).  The contract: with a = min(|v|, 6),
+// E2M1 stochastic rounding of one value v with its random word w, as the
+// grid value it rounds to (sign kept).  The contract: with a = min(|v|, 6),
 // lo <= a < hi the neighbouring grid points, frac = (a - lo) / (hi - lo) and
-// u = w >> 8, a goes up to hi iff u * 2^-24 < frac.
+// u = w >> 8, a goes up to hi iff u * 2^-24 < frac.  The encoders pass the
+// element's 16-bit random value h as w = h << 16 (see sr_words), so the
+// decision is h * 2^-16 < frac.
 //
 // Computed with directed rounding instead of a compare.  Let s = hi - lo be
 // the grid spacing of a's binade (0.5 below 2, otherwise half the binade's
@@ -268,10 +270,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& k) {
     return c;
 }
 
-// Random words of elements i0..i0+3 (i0 % 4 == 0) of a logical tensor for
-// stochastic rounding: counter (i0/4 low, i0/4 high, 0, 0), key = seed.
+// Random values of elements i0..i0+7 (i0 % 8 == 0) of a logical tensor for
+// stochastic rounding: one Philox block, key = seed, counter = (i0/8 low,
+// i0/8 high, 0, 0), read as eight 16-bit halves, low half of each word
+// first; element i0 + k takes half k.
 __device__ __forceinline__ uint4 sr_words(const PhiloxKey& key, uint64_t i0) {
-    uint64_t q = i0 >> 2;
+    uint64_t q = i0 >> 3;
     return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), key);
 }
 
@@ -286,10 +290,13 @@ __device__ __forceinline__ uint2 encode16(const float v[16], const PhiloxKey& ke
     } else {
         float y[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 r = sr_words(key, i0 + 4 * q);
-            e2m1_sr_pair(v[4 * q + 0], v[4 * q + 1], r.x, r.y, y[4 * q + 0], y[4 * q + 1]);
-            e2m1_sr_pair(v[4 * q + 2], v[4 * q + 3], r.z, r.w, y[4 * q + 2], y[4 * q + 3]);
+        for (int q = 0; q < 2; ++q) {
+            const uint4 r = sr_words(key, i0 + 8 * q);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // elements 8q + 2k (low half of word k) and 8q + 2k + 1 (high half)
+                e2m1_sr_pair(v[8 * q + 2 * k], v[8 * q + 2 * k + 1], w[k] << 16, w[k] & 0xFFFF0000u,
+                             y[8 * q + 2 * k], y[8 * q + 2 * k + 1]);
         }
         out.x = e2m1x8_rtn(y);  // exact: every y is a grid value
         out.y = e2m1x8_rtn(y + 8);
