@@ -169,9 +169,12 @@ def gpu_bench(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sr, rh = workloads.SR_SEED, workloads.RHT_SEED
 
-    # the step, op by op through the C ABI (the same calls nvfp4_linear_fwd/bwd make)
+    # the step, op by op through the C ABI (the same calls nvfp4_linear_fwd_rht
+    # and nvfp4_linear_bwd with X = NULL make)
     ops = [
-        ("quant_x_1x16_rtn", lambda: nv.nvfp4_quantize(x, out_rowwise=ctx.xq)),
+        # X rowwise (Fprop) and RHT colwise (Wgrad), RTN, both tensor amaxes from one read
+        ("quant_x_rtn_and_rht", lambda: nv.nvfp4_quantize_with_rht(x, round="rtn", rht_seed=rh, out_rowwise=ctx.xq,
+                                                                     out_colwise=ctx.xtq)),
         ("quant_w_16x16_both", lambda: nv.nvfp4_quantize(w, block="16x16", colwise=True, out_rowwise=ctx.wq,
                                                          out_colwise=ctx.wtq)),
         ("gemm_fprop", lambda: nv.nvfp4_gemm(ctx.xq, ctx.wq, out=y)),
@@ -179,21 +182,19 @@ def gpu_bench(args):
         ("quant_dy_sr_and_rht", lambda: nv.nvfp4_quantize_with_rht(dy, round="sr", seed=sr, rht_seed=rh,
                                                                      out_rowwise=ctx.dyq, out_colwise=ctx.dytq)),
         ("gemm_dgrad", lambda: nv.nvfp4_gemm(ctx.dyq, ctx.wtq, out=dx)),
-        ("rht_quant_x_rtn", lambda: nv.nvfp4_rht_quantize(x, round="rtn", rht_seed=rh, out_colwise=ctx.xtq)),
         ("gemm_wgrad", lambda: nv.nvfp4_gemm(ctx.dytq, ctx.xtq, out=dw)),
     ]
-    launches_per_op = {"quant_x_1x16_rtn": 2, "quant_w_16x16_both": 2, "gemm_fprop": 1, "quant_dy_sr_and_rht": 3,
-                       "gemm_dgrad": 1, "rht_quant_x_rtn": 2, "gemm_wgrad": 1}
+    launches_per_op = {"quant_x_rtn_and_rht": 3, "quant_w_16x16_both": 2, "gemm_fprop": 1, "quant_dy_sr_and_rht": 3,
+                       "gemm_dgrad": 1, "gemm_wgrad": 1}
     # algorithmic bytes: the amax pass reads the input once, the encode pass
     # reads it again and writes codes (1/2 byte per element) and one E4M3
     # scale per 16 elements per layout
     bx, bw, bdy = M * K * 2, N * K * 2, M * N * 2
     op_bytes = {
-        "quant_x_1x16_rtn": 2 * bx + M * K // 2 + M * K // 16,
-        "quant_w_16x16_both": 2 * bw + 2 * (N * K // 2 + N * K // 16),
         # one amax read, two encode reads, codes and scales of both layouts
+        "quant_x_rtn_and_rht": 3 * bx + 2 * (M * K // 2 + M * K // 16),
+        "quant_w_16x16_both": 2 * bw + 2 * (N * K // 2 + N * K // 16),
         "quant_dy_sr_and_rht": 3 * bdy + 2 * (M * N // 2 + M * N // 16),
-        "rht_quant_x_rtn": 2 * bx + M * K // 2 + M * K // 16,
     }
     gemm_flops = 2.0 * M * N * K
 
@@ -241,7 +242,7 @@ def gpu_bench(args):
     step_wall_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_evs), dev) / args.steps
     value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
 
-    # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd/bwd.
+    # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd_rht/bwd.
     # Every step copies its inputs X, W, dY from pinned host memory and its
     # results Y, dX, dW back.  The copies run on their own streams (one per
     # direction) and device buffers are double-buffered, so step i's results
@@ -275,10 +276,10 @@ def gpu_bench(args):
             stream.wait_event(ev["xw"][b])
             if i >= 2:
                 stream.wait_event(ev["out_free"][b])
-            nv.nvfp4_linear_fwd(xd, wd, ctx, Y=yd)
+            nv.nvfp4_linear_fwd(xd, wd, ctx, Y=yd, rht_seed=rh)       # also X^T's Wgrad codes
             ev["y"][b].record(stream)
             stream.wait_event(ev["dy"][b])
-            nv.nvfp4_linear_bwd(dyd, xd, ctx, sr_seed=sr, rht_seed=rh, dX=dxd, dW=dwd)
+            nv.nvfp4_linear_bwd(dyd, None, ctx, sr_seed=sr, rht_seed=rh, dX=dxd, dW=dwd)
             ev["bwd"][b].record(stream)
             ev["in_free"][b].record(stream)
             with torch.cuda.stream(d2h):
@@ -306,7 +307,7 @@ def gpu_bench(args):
                "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2 + dyh.numel() * 2),
                "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2 + dwh.numel() * 4),
-               "api": "nvfp4_linear_fwd + nvfp4_linear_bwd with pinned host buffers; copies on one stream per "
+               "api": "nvfp4_linear_fwd_rht + nvfp4_linear_bwd with pinned host buffers; copies on one stream per "
                       "direction, device buffers double-buffered so copies overlap the neighbouring steps' compute"}
     st = nv.nvfp4_sync_status()
     if st != nv.OK:
@@ -630,21 +631,21 @@ def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
         dw2 = torch.empty(d_model, d_ffn, dtype=torch.float32, device=dev)
 
         def lin(tag, c, xin, w, y):
-            return [(f"{tag}_quant_x", lambda: nv.nvfp4_quantize(xin, out_rowwise=c.xq)),
+            # X for Fprop and X^T (RHT) for Wgrad, one amax read (nvfp4_linear_fwd_rht)
+            return [(f"{tag}_quant_x", lambda: nv.nvfp4_quantize_with_rht(xin, round="rtn", rht_seed=rh,
+                                                                          out_rowwise=c.xq, out_colwise=c.xtq)),
                     (f"{tag}_quant_w", lambda: nv.nvfp4_quantize(w, block="16x16", colwise=True, out_rowwise=c.wq,
                                                                  out_colwise=c.wtq)),
                     (f"{tag}_gemm_fprop", lambda: nv.nvfp4_gemm(c.xq, c.wq, out=y))]
 
-        def lin_bwd(tag, c, dyin, xin, dxo, dwo):
+        def lin_bwd(tag, c, dyin, dxo, dwo):
             return [(f"{tag}_quant_dy", lambda: nv.nvfp4_quantize_with_rht(dyin, round="sr", seed=sr, rht_seed=rh,
                                                                            out_rowwise=c.dyq, out_colwise=c.dytq)),
                     (f"{tag}_gemm_dgrad", lambda: nv.nvfp4_gemm(c.dyq, c.wtq, out=dxo)),
-                    (f"{tag}_rht_quant_x", lambda: nv.nvfp4_rht_quantize(xin, round="rtn", rht_seed=rh,
-                                                                         out_colwise=c.xtq)),
                     (f"{tag}_gemm_wgrad", lambda: nv.nvfp4_gemm(c.dytq, c.xtq, out=dwo))]
 
-        ops = (lin("up", c1, x, w1, y1) + lin("down", c2, y1, w2, y2) + lin_bwd("down", c2, dy2, y1, dy1, dw2)
-               + lin_bwd("up", c1, dy1, x, dx, dw1))
+        ops = (lin("up", c1, x, w1, y1) + lin("down", c2, y1, w2, y2) + lin_bwd("down", c2, dy2, dy1, dw2)
+               + lin_bwd("up", c1, dy1, dx, dw1))
         nsteps = max(3, steps if m <= 8192 else steps // 2)
         per = _time_ops(nv, ops, flush, stream, nsteps)
         step_ms = sum(per.values()) / nsteps
@@ -653,17 +654,16 @@ def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
         quant_ms = step_ms - gemm_ms
         # algorithmic bytes of the quantize ops: amax read + encode read + codes and scales per layout
         bx, bh = m * d_model, m * d_ffn
-        qbytes = (2 * 2 * bx + bx * 9 // 16) + (2 * 2 * bh + bh * 9 // 16)            # quant_x of up, down
+        # X of up and down, and dY of down and up: each rowwise + RHT colwise from one amax read
+        qbytes = 2 * ((3 * 2 * bx + 2 * bx * 9 // 16) + (3 * 2 * bh + 2 * bh * 9 // 16))
         qbytes += 2 * (2 * 2 * d_model * d_ffn + 2 * d_model * d_ffn * 9 // 16)       # both W, 16x16 both layouts
-        qbytes += (3 * 2 * bx + 2 * bx * 9 // 16) + (3 * 2 * bh + 2 * bh * 9 // 16)   # dY of down, up (rowwise + RHT)
-        qbytes += (2 * 2 * bh + bh * 9 // 16) + (2 * 2 * bx + bx * 9 // 16)           # RHT X^T of down, up
         gemm_tf = 6 * 2.0 * m * d_model * d_ffn / (gemm_ms * 1e-3) / 1e12
         quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
         out[str(m)] = {"ms_per_step": round(step_ms, 4), "tflops": round(flops / (step_ms * 1e-3) / 1e12, 1),
                        "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tf, 1),
                        "gemm_frac": round(gemm_tf / fp4_peak, 4), "quant_ms": round(quant_ms, 4),
                        "quant_gbs": round(quant_gbs, 1), "quant_frac": round(quant_gbs / peaks["hbm"], 4),
-                       "steps": nsteps, "gpu_launches_per_step": 24,
+                       "steps": nsteps, "gpu_launches_per_step": 22,
                        "ops_ms": {k: round(v / nsteps, 4) for k, v in per.items()}}
         del x, w1, w2, dy2, c1, c2, y1, y2, dy1, dx, dw1, dw2, ops
         torch.cuda.empty_cache()

@@ -325,6 +325,8 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
  * for nvfp4_quantize_with_rht).  X, W, dY are bf16,
  * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
  * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).
+ * X may be NULL in nvfp4_linear_bwd when xtq already holds X^T's codes
+ * (nvfp4_linear_fwd_rht below).
  * dw_accumulate = 0: dW = dY^T X (FP32, overwritten); nonzero: the Wgrad
  * GEMM adds into dW (FP32 gradient accumulation across micro-batches, with
  * the GEMM's NVFP4_OUT_FP32_ADD).
@@ -345,6 +347,23 @@ typedef struct {
 nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
 nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,
                               uint64_t rht_seed, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_linear_fwd_rht -- nvfp4_linear_fwd that also quantizes Wgrad's X
+ * operand: X^T -> xtq (the 16-point RHT along the tokens with rht_seed, RTN),
+ * from the same read of X that gives xq's tensor scale
+ * (nvfp4_quantize_with_rht), so X's full-tensor amax scan runs once per step
+ * instead of twice (paper page, limitations paragraph: the tensor scale
+ * costs an extra full-tensor amax scan).  xq, xtq, Y are bit for bit what
+ * nvfp4_linear_fwd and the backward's own X^T quantization give.
+ * nvfp4_linear_bwd then takes X = NULL and reads xtq as it is; its rht_seed
+ * must be the one given here (both Wgrad operands share the sign vector).
+ * A caller that runs several forwards before their backwards keeps one xtq
+ * per forward (xq, wq, wtq may be shared: Dgrad reads only wtq, a function
+ * of W).  Errors: as nvfp4_linear_fwd, plus xtq's shape check.
+ */
+nvfp4_status nvfp4_linear_fwd_rht(const void* X, const void* W, void* Y, uint64_t rht_seed, nvfp4_linear_ctx* ctx,
+                                  nvfp4_stream_t stream);
 
 /* Bound, in nanoseconds, of every wait inside the GEMM kernels (a pipeline
  * stage that never fills, a barrier that never completes): past it the

@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_gemm_bf16.argtypes = [vp, i64, vp, i64, vp, st, i64, i64, i64, i64, vp]
             L.nvfp4_linear_fwd.restype = st
             L.nvfp4_linear_fwd.argtypes = [vp, vp, vp, ctypes.POINTER(nvfp4_linear_ctx), vp]
+            L.nvfp4_linear_fwd_rht.restype = st
+            L.nvfp4_linear_fwd_rht.argtypes = [vp, vp, vp, u64, ctypes.POINTER(nvfp4_linear_ctx), vp]
             L.nvfp4_linear_bwd.restype = st
             L.nvfp4_linear_bwd.argtypes = [vp, vp, vp, vp, u64, u64, ctypes.POINTER(nvfp4_linear_ctx), vp]
             L.nvfp4_set_wait_limit_ns.restype = ctypes.c_uint64
@@ -387,23 +389,31 @@ class LinearContext:
 
 
 def nvfp4_linear_fwd(X: torch.Tensor, W: torch.Tensor, ctx: LinearContext, Y: torch.Tensor | None = None,
-                     stream=None) -> torch.Tensor:
+                     stream=None, rht_seed: int | None = None) -> torch.Tensor:
+    """Y = X W^T.  With rht_seed: nvfp4_linear_fwd_rht, which also fills
+    ctx.xtq (X^T after the RHT, for Wgrad) from the same read of X; the
+    backward then takes X=None."""
     if Y is None:
         Y = torch.empty(ctx.M, ctx.N, dtype=torch.bfloat16, device=X.device)
     for t, shape in ((X, (ctx.M, ctx.K)), (W, (ctx.N, ctx.K)), (Y, (ctx.M, ctx.N))):
         if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_contiguous():
             raise ValueError(f"expected contiguous bf16 {shape}, got {t.dtype} {tuple(t.shape)}")
     c = ctx.c()
-    _check(lib().nvfp4_linear_fwd(X.data_ptr(), W.data_ptr(), Y.data_ptr(), ctypes.byref(c), _stream(stream)),
-           "nvfp4_linear_fwd")
+    if rht_seed is None:
+        _check(lib().nvfp4_linear_fwd(X.data_ptr(), W.data_ptr(), Y.data_ptr(), ctypes.byref(c), _stream(stream)),
+               "nvfp4_linear_fwd")
+    else:
+        _check(lib().nvfp4_linear_fwd_rht(X.data_ptr(), W.data_ptr(), Y.data_ptr(), int(rht_seed), ctypes.byref(c),
+                                          _stream(stream)), "nvfp4_linear_fwd_rht")
     return Y
 
 
-def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor, ctx: LinearContext, sr_seed: int, rht_seed: int,
+def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor | None, ctx: LinearContext, sr_seed: int, rht_seed: int,
                      dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None,
                      accumulate_dw: bool = False):
     """Dgrad and Wgrad of the layer; with accumulate_dw=True the FP32 Wgrad
-    result is added into the given dW instead of overwriting it."""
+    result is added into the given dW instead of overwriting it.  X=None:
+    ctx.xtq already holds X^T's codes (nvfp4_linear_fwd with rht_seed)."""
     if dX is None:
         dX = torch.empty(ctx.M, ctx.K, dtype=torch.bfloat16, device=dY.device)
     if dW is None:
@@ -412,11 +422,13 @@ def nvfp4_linear_bwd(dY: torch.Tensor, X: torch.Tensor, ctx: LinearContext, sr_s
         dW = torch.empty(ctx.N, ctx.K, dtype=torch.float32, device=dY.device)
     for t, shape, dt in ((dY, (ctx.M, ctx.N), torch.bfloat16), (X, (ctx.M, ctx.K), torch.bfloat16),
                          (dX, (ctx.M, ctx.K), torch.bfloat16), (dW, (ctx.N, ctx.K), torch.float32)):
+        if t is None:
+            continue
         if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
             raise ValueError(f"expected contiguous {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
     c = ctx.c(dw_accumulate=accumulate_dw)
-    _check(lib().nvfp4_linear_bwd(dY.data_ptr(), X.data_ptr(), dX.data_ptr(), dW.data_ptr(), sr_seed, rht_seed,
-                                  ctypes.byref(c), _stream(stream)), "nvfp4_linear_bwd")
+    _check(lib().nvfp4_linear_bwd(dY.data_ptr(), None if X is None else X.data_ptr(), dX.data_ptr(), dW.data_ptr(),
+                                  sr_seed, rht_seed, ctypes.byref(c), _stream(stream)), "nvfp4_linear_bwd")
     return dX, dW
 
 

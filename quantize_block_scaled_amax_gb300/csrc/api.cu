@@ -496,7 +496,11 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
     return check_launch("transpose_bf16");
 }
 
-nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
+namespace {
+// The forward pass; with_rht: X^T's RHT codes (xtq) as well, from the same
+// amax read of X.
+nvfp4_status linear_fwd(const void* X, const void* W, void* Y, bool with_rht, uint64_t rht_seed,
+                        nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
     g_err[0] = 0;
     if (!ctx || !X || !W || !Y) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
     const int64_t M = ctx->M, N = ctx->N, K = ctx->K;
@@ -506,19 +510,37 @@ nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linea
     if ((st = check_linear_tensor(&ctx->xq, M, K, "xq")) || (st = check_linear_tensor(&ctx->wq, N, K, "wq")) ||
         (st = check_linear_tensor(&ctx->wtq, K, N, "wtq")))
         return st;
-    if ((st = nvfp4_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_BLOCK_1x16, NVFP4_RTN, 0, &ctx->xq, nullptr,
-                             ctx->workspace, ctx->workspace_bytes, stream)))
+    if (with_rht) {
+        if ((st = check_linear_tensor(&ctx->xtq, K, M, "xtq"))) return st;
+        // X 1x16 RTN for Fprop and X^T after the RHT along the tokens, RTN,
+        // for Wgrad: both tensor scales from one read of X
+        if ((st = nvfp4_quantize_with_rht(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xq, &ctx->xtq,
+                                          ctx->workspace, ctx->workspace_bytes, stream)))
+            return st;
+    } else if ((st = nvfp4_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_BLOCK_1x16, NVFP4_RTN, 0, &ctx->xq, nullptr,
+                                    ctx->workspace, ctx->workspace_bytes, stream))) {
         return st;
+    }
     if ((st = nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq,
                              ctx->workspace, ctx->workspace_bytes, stream)))
         return st;
     return nvfp4_gemm(&ctx->xq, &ctx->wq, Y, NVFP4_OUT_BF16, N, nullptr, 0, stream);
 }
+}  // namespace
+
+nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
+    return linear_fwd(X, W, Y, false, 0, ctx, stream);
+}
+
+nvfp4_status nvfp4_linear_fwd_rht(const void* X, const void* W, void* Y, uint64_t rht_seed, nvfp4_linear_ctx* ctx,
+                                  nvfp4_stream_t stream) {
+    return linear_fwd(X, W, Y, true, rht_seed, ctx, stream);
+}
 
 nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,
                               uint64_t rht_seed, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
     g_err[0] = 0;
-    if (!ctx || !dY || !X || !dX || !dW) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    if (!ctx || !dY || !dX || !dW) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
     const int64_t M = ctx->M, N = ctx->N, K = ctx->K;
     if (M <= 0 || N <= 0 || K <= 0 || M % 64 || N % 64 || K % 64)
         return fail(NVFP4_ERR_INVALID_ARG, "M, N, K must be positive multiples of 64");
@@ -534,8 +556,9 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
     // Dgrad: dX = dY W with the 16x16 weight codes of W^T
     if ((st = nvfp4_gemm(&ctx->dyq, &ctx->wtq, dX, NVFP4_OUT_BF16, K, nullptr, 0, stream))) return st;
     // Wgrad: dW = dY^T X with both operands transformed along the tokens
-    if ((st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
-                                 ctx->workspace_bytes, stream)))
+    // (X null: xtq already holds X^T's codes from nvfp4_linear_fwd_rht)
+    if (X && (st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
+                                      ctx->workspace_bytes, stream)))
         return st;
     return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, ctx->dw_accumulate ? NVFP4_OUT_FP32_ADD : NVFP4_OUT_FP32, K, nullptr,
                       0, stream);

@@ -23,6 +23,12 @@ zeroes it between steps) inside the Wgrad GEMM itself, and leaves
 ``weight.grad`` unset; otherwise ``weight.grad`` gets the Wgrad result cast
 to the weight's dtype.
 
+Saved state: the forward quantizes X twice from one read of it (1x16 RTN
+for Fprop, and X^T after the RHT, RTN, for Wgrad: the C ABI's
+``nvfp4_linear_fwd_rht``), and keeps only the Wgrad operand for the
+backward, a fresh buffer per forward: 0.5625 bytes per element of X instead
+of X's 2.  Several forwards may run before their backwards.
+
 Precision: the paper page keeps some linear layers in BF16 (the last blocks
 of the network) and switches the whole model to BF16 for the final part of
 training to close the remaining loss gap.  A layer's ``precision`` is
@@ -38,7 +44,7 @@ import threading
 
 import torch
 
-from . import LinearContext, nvfp4_gemm_bf16, nvfp4_linear_bwd, nvfp4_linear_fwd, nvfp4_transpose_bf16
+from . import LinearContext, empty_qtensor, nvfp4_gemm_bf16, nvfp4_linear_bwd, nvfp4_linear_fwd, nvfp4_transpose_bf16
 
 __all__ = ["NVFP4LinearFunction", "BF16LinearFunction", "NVFP4Linear", "nvfp4_linear", "set_precision"]
 
@@ -104,8 +110,10 @@ class NVFP4LinearFunction(torch.autograd.Function):
         m, k = x2.shape
         n = w.shape[0]
         lc = contexts.get(m, n, k, x2.device)
-        y = nvfp4_linear_fwd(x2, w, lc)
-        ctx.save_for_backward(x2)
+        # this forward's X^T codes, kept for its own backward
+        lc.xtq = empty_qtensor(k, m, x2.device)
+        y = nvfp4_linear_fwd(x2, w, lc, rht_seed=rht_seed)
+        ctx.xtq = lc.xtq
         ctx.lc = lc
         ctx.lead = lead
         ctx.seeds = seeds
@@ -116,17 +124,16 @@ class NVFP4LinearFunction(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, dy):
-        (x2,) = ctx.saved_tensors
         lc = ctx.lc
         dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
-        # linear_fwd quantized W into lc.wtq, which Dgrad reads; a later forward
-        # through the same context must not run before this backward is done,
-        # which the stream order guarantees for single-stream training.
+        # Dgrad reads lc.wtq, which every forward of this layer writes from
+        # the same W; Wgrad reads this forward's own X^T codes
+        lc.xtq = ctx.xtq
         if ctx.main_grad is not None:
-            dx, _ = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed,
+            dx, _ = nvfp4_linear_bwd(dy2, None, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed,
                                      dW=ctx.main_grad, accumulate_dw=True)
             return dx.reshape(*ctx.lead, lc.K), None, None, None, None, None
-        dx, dw = nvfp4_linear_bwd(dy2, x2, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed)
+        dx, dw = nvfp4_linear_bwd(dy2, None, lc, sr_seed=ctx.seeds.take(), rht_seed=ctx.rht_seed)
         return dx.reshape(*ctx.lead, lc.K), dw.to(ctx.w_dtype), None, None, None, None
 
 

@@ -216,6 +216,13 @@ def test_linear_argument_checks_need_no_gpu(L):
     assert fwd(ctx(wtq=t(N, K))) == q.ERR_INVALID_ARG                                 # wtq is [K][N]
     assert b"wtq" in L.nvfp4_last_error()
 
+    # the forward that also writes Wgrad's X^T codes checks xtq as well
+    fwd_rht = lambda c, x=16: L.nvfp4_linear_fwd_rht(x, 16, 16, 5, ctypes.byref(c) if c is not None else None, None)
+    assert fwd_rht(None) == q.ERR_INVALID_ARG                                         # no context
+    assert fwd_rht(ctx(), x=None) == q.ERR_INVALID_ARG                                # null X
+    assert fwd_rht(ctx(xtq=t(N, M))) == q.ERR_INVALID_ARG                             # xtq is [K][M]
+    assert b"xtq" in L.nvfp4_last_error()
+
     bwd = lambda c, dw=16: L.nvfp4_linear_bwd(16, 16, 16, dw, 1, 2, ctypes.byref(c), None)
     assert bwd(ctx(), dw=None) == q.ERR_INVALID_ARG                                   # null dW
     assert bwd(ctx(K=0)) == q.ERR_INVALID_ARG                                         # empty

@@ -54,3 +54,30 @@ def test_linear_fwd_bwd(nv, mnk):
     # fidelity to the unquantized layer (a loose sanity bound, not parity)
     yr = xn.astype(np.float64) @ wn.astype(np.float64).T
     assert np.linalg.norm(y.float().cpu().numpy() - yr) / np.linalg.norm(yr) < 0.2
+
+
+def test_forward_with_rht_matches_the_two_pass_layer(nv):
+    # nvfp4_linear_fwd_rht quantizes X^T for Wgrad in the forward, from the
+    # same read of X as xq; the backward then takes X = NULL.  Every
+    # quantized operand and Y, dX, dW must equal the plain forward and the
+    # backward's own X^T quantization bit for bit.
+    m, n, k = 256, 384, 320
+    x, w, dy = workloads.linear_layer(m, n, k)
+    x, w, dy = x.cuda(), w.cuda(), dy.cuda()
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    a = nv.LinearContext(m, n, k, "cuda")
+    ya = nv.nvfp4_linear_fwd(x, w, a)
+    dxa, dwa = nv.nvfp4_linear_bwd(dy, x, a, sr_seed=sr, rht_seed=rh)
+    b = nv.LinearContext(m, n, k, "cuda")
+    yb = nv.nvfp4_linear_fwd(x, w, b, rht_seed=rh)
+    xtq_fwd = b.xtq.codes.clone()
+    dxb, dwb = nv.nvfp4_linear_bwd(dy, None, b, sr_seed=sr, rht_seed=rh)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    assert torch.equal(xtq_fwd, b.xtq.codes)        # the backward left xtq as the forward wrote it
+    for name in ("xq", "wq", "wtq", "dyq", "dytq", "xtq"):
+        qa, qb = getattr(a, name), getattr(b, name)
+        assert torch.equal(qa.codes, qb.codes) and torch.equal(qa.scales, qb.scales), name
+        assert torch.equal(qa.amax[:3], qb.amax[:3]), name      # {A, S_dec, S_enc}
+    assert torch.equal(ya, yb) and torch.equal(dxa, dxb) and torch.equal(dwa, dwb)
+    assert_quant_equal(b.xtq, oracle.quantize(to_f32_np(x), layout="col", rht_seed=rh), what="xtq from the forward")

@@ -135,3 +135,31 @@ def test_gemm_accumulate_into_fp32(nv):
     assert np.array_equal(c.cpu().numpy().view(np.uint32), expect.view(np.uint32))
     with pytest.raises(ValueError):
         nv.nvfp4_gemm(qa, qb, out=torch.empty(m, n, dtype=torch.bfloat16, device="cuda"), accumulate=True)
+
+
+def test_two_forwards_before_their_backwards(nv):
+    # micro-batches whose forwards both run before either backward (as in a
+    # pipelined schedule): each backward must use its own forward's X^T codes
+    from quantize_block_scaled_amax_gb300.linear import NVFP4Linear
+    m, n, k = 256, 384, 320
+    x1, w, dy1 = workloads.linear_layer(m, n, k)
+    x2 = workloads.activations(m, k, seed=workloads.SEED_BASE + 50)
+    dy2 = workloads.gradients(m, n, seed=workloads.SEED_BASE + 51)
+    layer = NVFP4Linear(k, n, device="cuda", seed_base=31, rht_seed=9)
+    with torch.no_grad():
+        layer.weight.copy_(w.cuda())
+    xa, xb = x1.cuda().requires_grad_(True), x2.cuda().requires_grad_(True)
+    ya, yb = layer(xa), layer(xb)
+    yb.backward(dy2.cuda())                          # seed 31
+    g_b = layer.weight.grad.clone()
+    layer.weight.grad = None
+    ya.backward(dy1.cuda())                          # seed 32
+    g_a = layer.weight.grad.clone()
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    wn = to_f32_np(w)
+    for xx, dd, seed, g, gx, tag in ((x2, dy2, 31, g_b, xb.grad, "second forward"),
+                                     (x1, dy1, 32, g_a, xa.grad, "first forward")):
+        d, _, dx_ref, dw_ref = _oracle_layer(to_f32_np(xx), wn, to_f32_np(dd), sr_seed=seed, rht_seed=9)
+        assert_gemm_close(gx.float().cpu().numpy(), dx_ref, d["dy"], d["wt"], bf16=True, what=f"dX, {tag}")
+        assert_gemm_close(g.float().cpu().numpy(), dw_ref, d["dyt"], d["xt"], bf16=True, what=f"dW, {tag}")
