@@ -65,9 +65,10 @@ def _peaks():
 
 # ---- profile summaries: DRAM traffic of the dominant kernel ------------------------
 
-def _profile_traffic(kernel_file: str, summary: str):
-    """Bytes per launch from a committed ncu summary, or None if the summary is
-    missing or was taken on a different version of the kernel source."""
+def _profile_traffic(summary: str, sources: tuple, field: str):
+    """DRAM bytes from a committed ncu summary (its `field` line), or None if
+    the summary is missing or any of the kernel sources it was taken on
+    (its `source_sha256 <file>: <hash>` lines) has changed since."""
     path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
@@ -76,11 +77,12 @@ def _profile_traffic(kernel_file: str, summary: str):
         if ":" in line and not line.startswith(" "):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = open(os.path.join(ROOT, "quantize_block_scaled_amax_gb300", "csrc", kernel_file), "rb").read()
-    if fields.get("source_sha256", "") != hashlib.sha256(src).hexdigest():
-        return None
+    for name in sources:
+        src = open(os.path.join(ROOT, "quantize_block_scaled_amax_gb300", "csrc", name), "rb").read()
+        if fields.get(f"source_sha256 {name}", "") != hashlib.sha256(src).hexdigest():
+            return None
     try:
-        return float(fields["dram_bytes_per_launch_full_size"])
+        return float(fields[field])
     except (KeyError, ValueError):
         return None
 
@@ -347,12 +349,18 @@ def gpu_bench(args):
     gemm_ach = gemm_flops / (gemm_avg_ms * 1e-3) / 1e12
     roof_gemm = {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                  "frac": round(gemm_ach / fp4_peak, 4),
-                 "traffic": _profile_traffic("gemm.cu", "gemm_nvf4_fprop_8192x20480x5120.txt"),
+                 # DRAM bytes per launch (ncu, average of the three GEMM launches)
+                 "traffic": _profile_traffic("gemm_nvf4_layer_gemms_dram_8192x20480x5120.txt", ("gemm.cu",),
+                                             "dram_bytes_per_launch_full_size"),
                  "kernel": "nvf4_gemm_kernel (avg of Fprop, Dgrad, Wgrad launches)",
                  "peak_source": f"{peaks['source']} burst bf16 {peaks['bf16']} TFLOP/s x "
                                 f"{FP4_OVER_BF16:g} (nominal FP4/BF16 ratio)"}
+    # DRAM bytes of all the step's quantize launches (ncu, cold cache per kernel)
+    quant_traffic = _profile_traffic("quantize_step_dram_8192x20480x5120.txt", ("quantize.cu", "nvfp4_device.cuh"),
+                                     "dram_bytes_per_step")
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
-                  "frac": round(quant_gbs / peaks["hbm"], 4), "traffic": None,
+                  "frac": round(quant_gbs / peaks["hbm"], 4), "traffic": quant_traffic,
+                  "traffic_unit": "bytes per step (all quantize launches)",
                   "kernel": "all quantize + RHT launches of the step (amax pass + encode pass)",
                   "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     dominant_is_gemm = gemm_ms >= quant_ms
