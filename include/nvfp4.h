@@ -62,7 +62,9 @@ typedef enum {
     NVFP4_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
     NVFP4_ERR_NONFINITE = 4,   /* (device) the input held a NaN or an infinity  */
     NVFP4_ERR_TIMEOUT = 5,     /* (device) a bounded pipeline wait ran out      */
-    NVFP4_ERR_CUDA = 6         /* a CUDA runtime call failed                    */
+    NVFP4_ERR_CUDA = 6,        /* a CUDA runtime call failed                    */
+    NVFP4_ERR_BOUNDS = 7       /* (device, checked build only) an index fell
+                                  outside its tensor; the access was skipped   */
 } nvfp4_status;
 
 typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
@@ -375,9 +377,30 @@ nvfp4_status nvfp4_linear_fwd_rht(const void* X, const void* W, void* Y, uint64_
 uint64_t nvfp4_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Synchronize `stream`, then return and clear the device status word of the
- * current device: NVFP4_ERR_NONFINITE, NVFP4_ERR_TIMEOUT or NVFP4_OK
- * (NVFP4_ERR_CUDA if the synchronization itself failed). */
+ * current device: NVFP4_ERR_BOUNDS (checked build), NVFP4_ERR_TIMEOUT,
+ * NVFP4_ERR_NONFINITE or NVFP4_OK, the first that applies (NVFP4_ERR_CUDA if
+ * the synchronization itself failed). */
 nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream);
+
+/*
+ * The checked build.  Compiled with -DNVFP4_CHECKED, every kernel of this
+ * library tests the index of each global-memory access it computes itself
+ * (input elements, codes, scale bytes, amax partials, scale atoms read by the
+ * GEMM) against its tensor's extent; an index outside it skips the access and
+ * sets NVFP4_ERR_BOUNDS in the status word.  (Compute sanitizers do not run
+ * everywhere this library does; this build answers the same question for the
+ * library's own index arithmetic.)  TMA copies are bounded by their tensor
+ * maps and are not checked again.
+ * nvfp4_checked_build returns 1 in the checked build, 0 otherwise.
+ * nvfp4_checked_selftest (checked build) runs one kernel whose single guarded
+ * store has an index one past its buffer by construction, so the check must
+ * skip it and report it; it returns what nvfp4_sync_status then returns
+ * (NVFP4_ERR_BOUNDS when the checks work) after verifying that the buffer's
+ * guard word was not written.  In the normal build it returns
+ * NVFP4_ERR_UNSUPPORTED without launching anything.
+ */
+int32_t nvfp4_checked_build(void);
+nvfp4_status nvfp4_checked_selftest(nvfp4_stream_t stream);
 
 /* Static English text of a status code. */
 const char* nvfp4_status_string(nvfp4_status status);

@@ -23,10 +23,11 @@ __all__ = [
     "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
     "nvfp4_transpose_bf16",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_set_wait_limit_ns", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_checked_build", "nvfp4_checked_selftest",
     "empty_qtensor", "scales_as_linear",
 ]
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA = range(7)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_BOUNDS = range(8)
 IN_BF16, IN_FP32 = 0, 1
 OUT_BF16, OUT_FP32, OUT_FP32_ADD = 0, 1, 2
 BLOCK_1x16, BLOCK_16x16, BLOCK_MX1x32 = 0, 1, 2
@@ -78,6 +79,10 @@ def lib() -> ctypes.CDLL:
             i64 = ctypes.c_int64
             u64 = ctypes.c_uint64
             tp = ctypes.POINTER(nvfp4_tensor)
+            L.nvfp4_checked_build.restype = ctypes.c_int32
+            L.nvfp4_checked_build.argtypes = []
+            L.nvfp4_checked_selftest.restype = st
+            L.nvfp4_checked_selftest.argtypes = [vp]
             L.nvfp4_scales_bytes.restype = ctypes.c_size_t
             L.nvfp4_scales_bytes.argtypes = [i64, i64, ctypes.c_int32]
             L.nvfp4_workspace_size.restype = ctypes.c_size_t
@@ -441,6 +446,17 @@ def nvfp4_set_wait_limit_ns(limit_ns: int) -> int:
 def nvfp4_sync_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device status code."""
     return int(lib().nvfp4_sync_status(_stream(stream)))
+
+
+def nvfp4_checked_build() -> bool:
+    """True when the loaded library is the checked build (NVFP4_CHECKED=1)."""
+    return bool(lib().nvfp4_checked_build())
+
+
+def nvfp4_checked_selftest(stream=None) -> int:
+    """Checked build: one guarded store past its buffer must be skipped and
+    reported (returns ERR_BOUNDS); ERR_UNSUPPORTED in the normal build."""
+    return int(lib().nvfp4_checked_selftest(_stream(stream)))
 
 
 def scales_as_linear(q: QTensor) -> torch.Tensor:

@@ -3,6 +3,12 @@
 Each translation unit under ``csrc/`` compiles in parallel to an object in
 ``_build/``; they link into ``_build/libnvfp4_gb300.so``.  No CMake, no torch
 extension machinery: the library is a plain C-ABI shared object.
+
+With the environment variable ``NVFP4_CHECKED=1`` the same sources build the
+checked library instead (``-DNVFP4_CHECKED``: every kernel tests the indices
+of the global-memory accesses it computes and reports a stray one as
+NVFP4_ERR_BOUNDS) into ``_build_checked/libnvfp4_gb300_checked.so``, and the
+binding loads that one.
 """
 from __future__ import annotations
 
@@ -14,8 +20,9 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-BUILD = os.path.join(HERE, "_build")
-LIB = os.path.join(BUILD, "libnvfp4_gb300.so")
+CHECKED = os.environ.get("NVFP4_CHECKED", "") not in ("", "0")
+BUILD = os.path.join(HERE, "_build_checked" if CHECKED else "_build")
+LIB = os.path.join(BUILD, "libnvfp4_gb300_checked.so" if CHECKED else "libnvfp4_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -47,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + (["-DNVFP4_CHECKED"] if CHECKED else []) + list(extra_flags or [])
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")

@@ -16,6 +16,18 @@ namespace nvfp4 {
 // Per-device status word (NVFP4_ERR_NONFINITE / NVFP4_ERR_TIMEOUT bits).
 static __device__ uint32_t g_status_word;
 
+#ifdef NVFP4_CHECKED
+// nvfp4_checked_selftest: a two-word logical buffer followed by a guard word
+// in the same array, and one guarded store whose index is one past the
+// logical buffer (so even an unchecked store would land on the guard word).
+static __device__ uint32_t g_selftest_words[3];
+static __global__ void checked_selftest_kernel(uint32_t* status) {
+    const int64_t n = 2;
+    const int64_t i = n;  // one past the logical buffer, by construction
+    if (NVFP4_IN_BOUNDS(i < n, status)) g_selftest_words[i] = 0xFFFFFFFFu;
+}
+#endif
+
 namespace {
 
 thread_local char g_err[512];
@@ -80,6 +92,7 @@ size_t scales_bytes(int64_t rows, int64_t cols, int32_t layout) {
 ScaleOut scale_out(const nvfp4_tensor& t) {
     ScaleOut s;
     s.p = t.scales;
+    s.bytes = (int64_t)scales_bytes(t.rows, t.cols, t.scale_layout);
     s.n_katoms = n_katoms(t.cols);
     s.nkb = t.cols / 16;
     s.mma = t.scale_layout == NVFP4_SCALES_MMA;
@@ -190,6 +203,7 @@ const char* nvfp4_status_string(nvfp4_status st) {
         case NVFP4_ERR_NONFINITE: return "non-finite input";
         case NVFP4_ERR_TIMEOUT: return "device wait timed out";
         case NVFP4_ERR_CUDA: return "CUDA error";
+        case NVFP4_ERR_BOUNDS: return "device index out of bounds (checked build)";
     }
     return "unknown status";
 }
@@ -637,9 +651,42 @@ nvfp4_status nvfp4_sync_status(nvfp4_stream_t stream) {
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
         if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemcpyToSymbol: %s", cudaGetErrorString(e));
     }
+    if (word & kStatusBounds) return fail(NVFP4_ERR_BOUNDS, "a device index fell outside its tensor (checked build)");
     if (word & kStatusTimeout) return fail(NVFP4_ERR_TIMEOUT, "a device wait ran out of iterations");
     if (word & kStatusNonfinite) return fail(NVFP4_ERR_NONFINITE, "input held a NaN or an infinity");
     return NVFP4_OK;
+}
+
+int32_t nvfp4_checked_build(void) {
+#ifdef NVFP4_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+nvfp4_status nvfp4_checked_selftest(nvfp4_stream_t stream) {
+    g_err[0] = 0;
+#ifndef NVFP4_CHECKED
+    (void)stream;
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_checked_selftest needs the checked build");
+#else
+    DeviceInfo* dev;
+    nvfp4_status st = device_info(&dev);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t zero[3] = {0u, 0u, 0u};
+    cudaError_t e = cudaMemcpyToSymbolAsync(g_selftest_words, zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemcpyToSymbolAsync: %s", cudaGetErrorString(e));
+    checked_selftest_kernel<<<1, 1, 0, s>>>(dev->status);
+    if ((st = check_launch("checked_selftest"))) return st;
+    st = nvfp4_sync_status(stream);
+    uint32_t words[3];
+    e = cudaMemcpyFromSymbol(words, g_selftest_words, sizeof words);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaMemcpyFromSymbol: %s", cudaGetErrorString(e));
+    if (words[2] != 0u) return fail(NVFP4_ERR_CUDA, "the guarded store past the buffer was not skipped");
+    return st;
+#endif
 }
 
 }  // extern "C"

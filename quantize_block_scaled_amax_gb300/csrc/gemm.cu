@@ -502,7 +502,6 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
         const int ga = 2 * mt + (int)rank;                // this CTA's A group
         const bool a_in = ga < p.a_groups;
         const int nb = min(2, p.b_groups - 2 * nt);       // B groups of the pair tile that exist
-        const uint32_t bytes = (uint32_t)((a_in ? 1 : 0) + nb) * kSfRunBytes;
         const uint8_t* a_src = p.a_scales + (size_t)ga * p.n_katoms * kSfAtomBytes;
         const uint8_t* b_src = p.b_scales + (size_t)(2 * nt) * p.n_katoms * kSfAtomBytes;
         const size_t b_group = (size_t)p.n_katoms * kSfAtomBytes;
@@ -512,9 +511,13 @@ __device__ __forceinline__ void scale_producer_role(const Params& p, SharedState
             if (!mbar_wait(&ss->empty[s], ph ^ 1u, ss, p.status, p.timeout_ns)) return;
             uint8_t* sf = stages + s * kStageBytes + kCodeBytes;
             const size_t k_off = (size_t)kt * kSfRunBytes;
-            mbar_arrive_expect_tx(&ss->sf_in[s], bytes);
-            if (a_in) bulk_load(sf, a_src + k_off, kSfRunBytes, &ss->sf_in[s]);
-            for (int g = 0; g < nb; ++g)
+            // a stage's run lies inside its 128-row group's atoms (checked build)
+            const bool k_in = NVFP4_IN_BOUNDS(k_off + kSfRunBytes <= b_group, p.status);
+            const bool a_ld = a_in && k_in;
+            const int nb_ld = k_in ? nb : 0;
+            mbar_arrive_expect_tx(&ss->sf_in[s], (uint32_t)((a_ld ? 1 : 0) + nb_ld) * kSfRunBytes);
+            if (a_ld) bulk_load(sf, a_src + k_off, kSfRunBytes, &ss->sf_in[s]);
+            for (int g = 0; g < nb_ld; ++g)
                 bulk_load(sf + (1 + g) * kSfRunBytes, b_src + g * b_group + k_off, kSfRunBytes, &ss->sf_in[s]);
         }
     }

@@ -18,6 +18,18 @@ constexpr float kFltMax = 3.402823466e+38f;
 // Bits of the per-device status word.
 constexpr uint32_t kStatusNonfinite = 1u;
 constexpr uint32_t kStatusTimeout = 2u;
+constexpr uint32_t kStatusBounds = 4u;
+
+// Device bounds checks of the checked build (compiled with -DNVFP4_CHECKED):
+// NVFP4_IN_BOUNDS(cond, status) is true when the index condition holds;
+// otherwise it records kStatusBounds in the status word (read back as
+// NVFP4_ERR_BOUNDS) and the caller skips the access.  In the normal build it
+// is the constant true and costs nothing.
+#ifdef NVFP4_CHECKED
+#define NVFP4_IN_BOUNDS(cond, status) ((cond) || (atomicOr((status), kStatusBounds), false))
+#else
+#define NVFP4_IN_BOUNDS(cond, status) true
+#endif
 
 // ---------------------------------------------------------------------------
 // Tensor scales from the tensor amax A (given as the bit pattern of |A|).
@@ -353,6 +365,7 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64
 
 struct ScaleOut {
     uint8_t* p;
+    int64_t bytes;     // the layout's size for this tensor (nvfp4_scales_bytes)
     int64_t n_katoms;  // MMA layout
     int64_t nkb;       // linear layout: blocks per row (cols / 16)
     int mma;

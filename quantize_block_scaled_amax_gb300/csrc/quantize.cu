@@ -398,7 +398,8 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
         bool ok[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            ok[h] = kb0 + 32 * h < bpr;
+            ok[h] = kb0 + 32 * h < bpr &&
+                    NVFP4_IN_BOUNDS(r >= 0 && r < rows && kb0 + 32 * h >= 0 && (kb0 + 32 * h) * 16 + 16 <= cols, status);
             if (ok[h]) blk[h].load(x + r * ldx + (kb0 + 32 * h) * 16);
         }
         uint32_t bm[2];
@@ -444,8 +445,10 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
                     c = encode16<kSR>(v, key, i0);
                 }
             }
-            *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
-            so.p[so.offset(r, kb)] = (uint8_t)sb;
+            if (NVFP4_IN_BOUNDS(kb * 8 + 8 <= ld_codes, status))
+                *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
+            const int64_t soff = so.offset(r, kb);
+            if (NVFP4_IN_BOUNDS(soff >= 0 && soff < so.bytes, status)) so.p[soff] = (uint8_t)sb;
         }
     }
 }
@@ -495,7 +498,8 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
         for (int k = 0; k < kLoads; ++k) {
             const int L = threadIdx.x + kColThreads * k;
             const int lr = L / kVecPerRow, seg = L % kVecPerRow;
-            if (r0 + lr < rows && c0 + seg * V < cols)
+            if (r0 + lr < rows && c0 + seg * V < cols &&
+                NVFP4_IN_BOUNDS(r0 + lr >= 0 && c0 + seg * V >= 0 && c0 + seg * V + V <= cols, status))
                 *reinterpret_cast<uint4*>(&tile[lr][seg * V]) =
                     __ldg(reinterpret_cast<const uint4*>(x + (r0 + lr) * ldx + c0 + seg * V));
         }
@@ -557,7 +561,11 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
                     }
                 }
             }
-            if (nb > 0) {
+            // output row oc of x^T holds `rows` codes; this thread's nb blocks
+            // from element orow0; its scale bytes from block orow0 / 16
+            if (nb > 0 && NVFP4_IN_BOUNDS(orow0 / 2 + 8 * nb <= ld_codes && orow0 + 16 * nb <= rows &&
+                                              so.offset(oc, orow0 / 16 + nb - 1) < so.bytes && so.offset(oc, orow0 / 16) >= 0,
+                                          status)) {
                 uint8_t* dst = codes + oc * ld_codes + orow0 / 2;
                 if (nb == 4) {
                     reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -727,6 +735,7 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
         return p;
     };
     auto load16 = [&](Quad<T>(&q)[16], const TilePos& p) {
+        if (!NVFP4_IN_BOUNDS(p.r >= 0 && p.r + 16 <= rows && p.col >= 0 && p.col + 4 <= cols, status)) return;
         const T* src = x + p.r * ldx + p.col;
 #pragma unroll
         for (int i = 0; i < 16; ++i) q[i].load(src + i * ldx);
@@ -760,7 +769,7 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
                 b23 = f32x2_mul(b23, r2);
                 const float a[4] = {f32x2_lo(a01), f32x2_hi(a01), f32x2_lo(a23), f32x2_hi(a23)};
                 const float b[4] = {f32x2_lo(b01), f32x2_hi(b01), f32x2_lo(b23), f32x2_hi(b23)};
-                if (codes_r && p.ok) {
+                if (codes_r && p.ok && NVFP4_IN_BOUNDS(p.r + i + 1 < rows && p.col / 2 + 2 <= ld_r, status)) {
                     const int64_t r = p.r + i;
                     const uint32_t ca = zero ? 0u : e2m1x4_rtn(a[0], a[1], a[2], a[3]);
                     const uint32_t cb = zero ? 0u : e2m1x4_rtn(b[0], b[1], b[2], b[3]);
@@ -777,19 +786,24 @@ __global__ void __launch_bounds__(k2dThreads, 2) quantize_2d_kernel(
                 }
             }
             if (p.ok) {
-                if (codes_r) {
+                if (codes_r && NVFP4_IN_BOUNDS(so_r.offset(p.r + 4 * qd, p.col / 16) >= 0 &&
+                                                   so_r.offset(p.r + 4 * qd, p.col / 16) + 3 * step_r < so_r.bytes,
+                                               status)) {
                     uint8_t* sp = so_r.p + so_r.offset(p.r + 4 * qd, p.col / 16);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) sp[k * step_r] = (uint8_t)bs.sb;
                 }
-                if (codes_c) {
+                if (codes_c && NVFP4_IN_BOUNDS(so_c.offset(p.col, p.r / 16) >= 0 &&
+                                                   so_c.offset(p.col, p.r / 16) + 3 * step_c < so_c.bytes,
+                                               status)) {
                     uint8_t* sp = so_c.p + so_c.offset(p.col, p.r / 16);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) sp[j * step_c] = (uint8_t)bs.sb;
                 }
             }
         }
-        if (t == U::kTiles - 1 && codes_c && p.valid && p.col < cols) {
+        if (t == U::kTiles - 1 && codes_c && p.valid && p.col < cols &&
+            NVFP4_IN_BOUNDS(p.col + 4 <= cols && (p.r - 16 * t) / 2 + 8 * U::kTiles <= ld_c, status)) {
             // the unit is done: 8 bytes of x^T per column and tile
             const int64_t r0 = p.r - 16 * t;
 #pragma unroll

@@ -38,6 +38,18 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_normal_build_has_no_bounds_checks(L):
+    # the checked build is a separate library (NVFP4_CHECKED=1); this one
+    # answers that it is not, and its self-test refuses before any launch
+    import quantize_block_scaled_amax_gb300 as q
+    from quantize_block_scaled_amax_gb300 import build
+    if build.CHECKED:
+        pytest.skip("this process runs the checked build")
+    assert L.nvfp4_checked_build() == 0
+    assert L.nvfp4_checked_selftest(None) == q.ERR_UNSUPPORTED
+    assert q.ERR_BOUNDS == 7 and L.nvfp4_status_string(q.ERR_BOUNDS).startswith(b"device index out of bounds")
+
+
 def test_struct_layout_matches_header(L, tmp_path):
     # the binding's ctypes structures against the C compiler's view of the
     # header: every field's offset and each struct's size
