@@ -205,30 +205,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// One blocking test that suspends the thread until the phase completes or
-// about `hint_ns` have passed.
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait for the phase with the given parity; false on abort or
-// timeout.  The thread sleeps in the barrier test for at most a quarter of
-// the bound (and at most 1 ms) at a time, then looks at the CTA's abort flag
-// and the clock.
+// timeout.  Each try_wait blocks for at most a system-dependent short time;
+// between them the thread looks at its CTA's abort flag and the clock.  (A
+// try_wait with a suspend-time hint woke its thread later after the phase
+// completed: the GEMM ran 3-6% slower with it.)
 __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, SharedState* ss, uint32_t* status,
                                             uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
-    const uint32_t hint = (uint32_t)(limit_ns / 4 < 1000000ull ? limit_ns / 4 : 1000000ull);
     for (;;) {
-        if (mbar_try_wait_for(bar, parity, hint)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*reinterpret_cast<volatile int*>(&ss->abort_flag)) return false;
         if (globaltimer() - t0 > limit_ns) {
             atomicOr(status, kStatusTimeout);
