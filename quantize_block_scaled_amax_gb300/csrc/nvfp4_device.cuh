@@ -204,51 +204,6 @@ __device__ __forceinline__ uint64_t x2_fma_rp(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
-// E2M1 stochastic rounding of one value v with its random word w, as the
-// grid value it rounds to (sign kept).  The contract: with a = min(|v|, 6),
-// lo <= a < hi the neighbouring grid points, frac = (a - lo) / (hi - lo) and
-// u = w >> 8, a goes up to hi iff u * 2^-24 < frac.  The encoders pass the
-// element's 16-bit random value h as w = h << 16 (see sr_words), so the
-// decision is h * 2^-16 < frac.
-//
-// Computed with directed rounding instead of a compare.  Let s = hi - lo be
-// the grid spacing of a's binade (0.5 below 2, otherwise half the binade's
-// power of two) and t = u * 2^-24.  Then lo + s * ceil(frac - t) is hi exactly
-// when frac > t, and ceil(frac - t) = ceil(a/s - t) - lo/s, so the rounded
-// value is s * ceil((a - s t) / s).  a - s t is formed by one FMA rounded
-// upward (s t is exact: a power of two times a 24-bit integer), and rounding
-// upward never moves a value past the next multiple of s (those are
-// representable), so the ceiling is unchanged; adding M = 1.5 * 2^23 * s,
-// whose binade has spacing s, rounded upward again, lands on M + that
-// multiple, and subtracting M is exact.  For |v| > 6 the result is >= 6 and
-// the saturating conversion gives code 7, which is what clamping to 6 first
-// gives; so no clamp is needed (|v| stays finite: |v| <= ~12 by construction
-// of the block scale).
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t w) {
-    // p = 2^max(e, 0) for |v| in [2^e, 2^(e+1)); s = p / 2
-    const float p = fmaxf(__uint_as_float(__float_as_uint(v) & 0x7F800000u), 1.0f);
-    const float uf = __uint2float_rn(w & 0xFFFFFF00u);  // u * 2^8, exact
-    const float z = __fmaf_ru(uf, __fmul_rn(p, -1.16415321826934814453125e-10f /* -2^-33 */), fabsf(v));
-    const float m = __fmul_rn(p, 6291456.0f);  // 1.5 * 2^22 * p = 1.5 * 2^23 * s
-    const float y = __fsub_rn(__fadd_ru(z, m), m);
-    return __uint_as_float(__float_as_uint(y) | (__float_as_uint(v) & 0x80000000u));
-}
-
-// e2m1_sr_value of two values at once: the FP steps on packed pairs (each
-// lane the same correctly rounded operation, directed roundings included).
-__device__ __forceinline__ void e2m1_sr_pair(float v0, float v1, uint32_t w0, uint32_t w1, float& y0, float& y1) {
-    const uint64_t p = x2_pack(fmaxf(__uint_as_float(__float_as_uint(v0) & 0x7F800000u), 1.0f),
-                               fmaxf(__uint_as_float(__float_as_uint(v1) & 0x7F800000u), 1.0f));
-    const uint64_t uf = x2_pack(__uint2float_rn(w0 & 0xFFFFFF00u), __uint2float_rn(w1 & 0xFFFFFF00u));
-    const uint64_t a = x2_pack(fabsf(v0), fabsf(v1));
-    const float c = -1.16415321826934814453125e-10f;  // -2^-33
-    const uint64_t z = x2_fma_rp(uf, x2_mul(p, x2_pack(c, c)), a);
-    const uint64_t m = x2_mul(p, x2_pack(6291456.0f, 6291456.0f));
-    const uint64_t y = x2_sub(x2_add_rp(z, m), m);
-    y0 = __uint_as_float(__float_as_uint(x2_lo(y)) | (__float_as_uint(v0) & 0x80000000u));
-    y1 = __uint_as_float(__float_as_uint(x2_hi(y)) | (__float_as_uint(v1) & 0x80000000u));
-}
-
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  Round i uses the key
 // (k0 + i * 0x9E3779B9, k1 + i * 0xBB67AE85); PhiloxKey holds the ten round
@@ -291,29 +246,89 @@ __device__ __forceinline__ uint4 sr_words(const PhiloxKey& key, uint64_t i0) {
     return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), key);
 }
 
-// Encode 16 consecutive elements of one block (already multiplied by r) into
-// 8 bytes.  SR: i0 is the logical index of element 0 (multiple of 16).
-template <bool kSR>
-__device__ __forceinline__ uint2 encode16(const float v[16], const PhiloxKey& key, uint64_t i0) {
+// E2M1 stochastic rounding.  The contract: with a = min(|v|, 6), lo <= a < hi
+// the neighbouring grid points, frac = (a - lo) / (hi - lo) and h the
+// element's 16-bit random value (see sr_words), a goes up to hi iff
+// h * 2^-16 < frac.
+//
+// Computed with directed rounding instead of a compare.  Let s = hi - lo be
+// the grid spacing of a's binade (0.5 below 2, otherwise half the binade's
+// power of two) and t = h * 2^-16.  Then lo + s * ceil(frac - t) is hi exactly
+// when frac > t, and ceil(frac - t) = ceil(a/s - t) - lo/s, so the rounded
+// value is s * ceil((a - s t) / s).  a - s t is formed by one FMA rounded
+// upward (s t is exact: a power of two times a 16-bit integer), and rounding
+// upward never moves a value past the next multiple of s (those are
+// representable), so the ceiling is unchanged; adding M = 1.5 * 2^23 * s,
+// whose binade has spacing s, rounded upward again, lands on M + that
+// multiple, and subtracting M is exact.  For |v| > 6 the result is >= 6 and
+// the saturating conversion gives code 7, which is what clamping to 6 first
+// gives; so no clamp is needed (|v| stays finite: |v| <= ~12 by construction
+// of the block scale).
+
+// Two elements at once, the FP steps on packed pairs (each lane the same
+// correctly rounded operation, directed roundings included): the scaled
+// magnitudes a0, a1 (>= 0) with the 16-bit random values h0 (low half of w)
+// and h1 (high half); the results take the signs of s0, s1.  p = 2^max(e, 0)
+// for a in [2^e, 2^(e+1)), so s = p / 2; uf = h exactly, and
+// uf * (p * -2^-17) = -s t; M = 1.5 * 2^22 * p.  The 16-bit halves go
+// straight into the conversions and |x| comes out of the scaling multiply
+// (encode16_scaled), which saves the logic operations that masked them.
+__device__ __forceinline__ void e2m1_sr_pair_mag(float a0, float a1, float s0, float s1, uint32_t w, float& y0,
+                                                 float& y1) {
+    const uint64_t p = x2_pack(fmaxf(__uint_as_float(__float_as_uint(a0) & 0x7F800000u), 1.0f),
+                               fmaxf(__uint_as_float(__float_as_uint(a1) & 0x7F800000u), 1.0f));
+    float u0, u1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f32.u16 %0, lo;\n\tcvt.rn.f32.u16 %1, hi;\n\t}"
+        : "=f"(u0), "=f"(u1)
+        : "r"(w));
+    const float c = -7.62939453125e-06f;  // -2^-17
+    const uint64_t z = x2_fma_rp(x2_pack(u0, u1), x2_mul(p, x2_pack(c, c)), x2_pack(a0, a1));
+    const uint64_t m = x2_mul(p, x2_pack(6291456.0f, 6291456.0f));
+    const uint64_t y = x2_sub(x2_add_rp(z, m), m);
+    y0 = __uint_as_float(__float_as_uint(x2_lo(y)) | (__float_as_uint(s0) & 0x80000000u));
+    y1 = __uint_as_float(__float_as_uint(x2_hi(y)) | (__float_as_uint(s1) & 0x80000000u));
+}
+
+// Encode 16 consecutive elements of one block (already multiplied by r, RTN)
+// into 8 bytes.
+__device__ __forceinline__ uint2 encode16_rtn(const float v[16]) {
     uint2 out;
+    out.x = e2m1x8_rtn(v);
+    out.y = e2m1x8_rtn(v + 8);
+    return out;
+}
+
+// Encode the 16 elements x[k] * r of one block (r > 0, each product rounded
+// as __fmul_rn) into 8 bytes.  SR: i0 is the logical index of element 0
+// (a multiple of 16); the magnitudes |x| * r come straight out of the
+// multiply and the signs from x, the same values as scaling first and taking
+// |v| after.
+template <bool kSR>
+__device__ __forceinline__ uint2 encode16_scaled(const float x[16], float r, const PhiloxKey& key, uint64_t i0) {
     if constexpr (!kSR) {
-        out.x = e2m1x8_rtn(v);
-        out.y = e2m1x8_rtn(v + 8);
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(x[k], r);
+        return encode16_rtn(v);
     } else {
         float y[16];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const uint4 r = sr_words(key, i0 + 8 * q);
-            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+            const uint4 rw = sr_words(key, i0 + 8 * q);
+            const uint32_t w[4] = {rw.x, rw.y, rw.z, rw.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // elements 8q + 2k (low half of word k) and 8q + 2k + 1 (high half)
-                e2m1_sr_pair(v[8 * q + 2 * k], v[8 * q + 2 * k + 1], w[k] << 16, w[k] & 0xFFFF0000u,
-                             y[8 * q + 2 * k], y[8 * q + 2 * k + 1]);
+            for (int k = 0; k < 4; ++k) {
+                const int e = 8 * q + 2 * k;
+                e2m1_sr_pair_mag(__fmul_rn(fabsf(x[e]), r), __fmul_rn(fabsf(x[e + 1]), r), x[e], x[e + 1], w[k], y[e],
+                                 y[e + 1]);
+            }
         }
+        uint2 out;
         out.x = e2m1x8_rtn(y);  // exact: every y is a grid value
         out.y = e2m1x8_rtn(y + 8);
+        return out;
     }
-    return out;
 }
 
 // 16-point random Hadamard transform of one chunk, in place:

@@ -269,9 +269,7 @@ __device__ __forceinline__ uint2 quantize_block(float v[16], const TensorScales&
     if (!ts.finite) bs.sb = 0u;
     sb_out = bs.sb;
     if (bs.sb == 0u) return make_uint2(0u, 0u);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
-    return encode16<kSR>(v, key, i0);
+    return encode16_scaled<kSR>(v, bs.r, key, i0);
 }
 
 // ---------------------------------------------------------------------------
@@ -351,10 +349,7 @@ __device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, co
     const uint32_t sb = mx_block_scale(__uint_as_float(bmax_bits));
     sb_out = sb;
     if (bmax_bits == 0u) return make_uint2(0u, 0u);
-    const float mul = mx_multiplier(sb);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], mul);
-    return encode16<kSR>(v, key, i0);
+    return encode16_scaled<kSR>(v, mx_multiplier(sb), key, i0);
 }
 
 // ---------------------------------------------------------------------------
@@ -439,11 +434,7 @@ __global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantiz
                 BlockScale bs = block_scale(__uint_as_float(bm[h]), ts.s_enc, r_tab);
                 if (!ts.finite) bs.sb = 0u;
                 sb = bs.sb;
-                if (bs.sb != 0u) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], bs.r);
-                    c = encode16<kSR>(v, key, i0);
-                }
+                if (bs.sb != 0u) c = encode16_scaled<kSR>(v, bs.r, key, i0);
             }
             if (NVFP4_IN_BOUNDS(kb * 8 + 8 <= ld_codes, status))
                 *reinterpret_cast<uint2*>(codes + r * ld_codes + kb * 8) = c;
