@@ -209,8 +209,17 @@ def gpu_bench(args):
     if st != nv.OK:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-           for _ in range(args.steps)]
+    # The timed step: the layer's two public calls, nvfp4_linear_fwd_rht (X
+    # and X^T's RHT codes from one amax read, W's 16x16 codes on the
+    # library's second stream meanwhile, Fprop) and nvfp4_linear_bwd with
+    # X = NULL (dY's SR codes, Dgrad, Wgrad): the same launches as the op list.
+    def layer_step():
+        nv.nvfp4_linear_fwd(x, w, ctx, Y=y, rht_seed=rh)
+        nv.nvfp4_linear_bwd(dy, None, ctx, sr_seed=sr, rht_seed=rh, dX=dx, dW=dw)
+
+    for _ in range(args.warmup):
+        layer_step()
+    torch.cuda.synchronize()
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
@@ -223,26 +232,35 @@ def gpu_bench(args):
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                  # evict L2 between steps (not timed)
         step_evs[s][0].record(stream)
-        for (name, fn), (e0, e1) in zip(ops, evs[s]):
-            e0.record(stream)
-            fn()
-            e1.record(stream)
+        layer_step()
         step_evs[s][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if rank == 0 else None
+    st = nv.nvfp4_sync_status()
+    if st != nv.OK:
+        raise RuntimeError(f"device status {st} after the timed steps")
+    ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_evs), dev) / args.steps
+    value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
 
+    # The same step op by op (one stream, an event pair around each op) for
+    # the per-kernel times, rooflines and shares.
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        for (name, fn), (e0, e1) in zip(ops, evs[s]):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
     per_op = {name: 0.0 for name, _ in ops}
     for s in range(args.steps):
         for (name, _), (e0, e1) in zip(ops, evs[s]):
             per_op[name] += e0.elapsed_time(e1)
-    total_ms = max_over_ranks(sum(per_op.values()), dev)
-    ms_per_step = total_ms / args.steps
-    # one event pair around each whole step as well: the per-op sum leaves out
-    # any idle time between the launches the host issues one by one
-    step_wall_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_evs), dev) / args.steps
-    value = world * 3 * gemm_flops / (ms_per_step * 1e-3) / 1e12
+    ops_ms_per_step = max_over_ranks(sum(per_op.values()), dev) / args.steps
 
     # ---- end to end: host buffers in, results back, through nvfp4_linear_fwd_rht/bwd.
     # Every step copies its inputs X, W, dY from pinned host memory and its
@@ -367,7 +385,7 @@ def gpu_bench(args):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "ms_per_step_wall": round(step_wall_ms, 4),
+        "ms_per_step_ops": round(ops_ms_per_step, 4),
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate; fp32 quantize)",
         "data": "synthetic (seeded: X N(0,1)+0.1% x50 outliers, W N(0,0.02), dY Student-t(3)*1e-3)",
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "l2": "flushed between steps (256 MB write)",
@@ -572,6 +590,26 @@ def _time_ops(nv, ops, flush, stream, steps):
     return per
 
 
+def _time_steps(nv, step, flush, stream, steps):
+    """Average CUDA-event milliseconds of `step` (3 untimed warm-up steps;
+    L2 flushed by a write before every step, outside the events)."""
+    import torch
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for st in range(steps):
+        flush.fill_(st & 0xFF)
+        evs[st][0].record(stream)
+        step()
+        evs[st][1].record(stream)
+    torch.cuda.synchronize()
+    status = nv.nvfp4_sync_status()
+    if status != nv.OK:
+        raise RuntimeError(f"device status {status} after timing a step")
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
 def rht_rows_measure(nv, x, w, dy, flush, stream, steps):
     """Quantization of the Fprop and Dgrad operands with the 16-point RHT
     along their K (the transform the pages leave optional there): X and W
@@ -654,12 +692,21 @@ def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
 
         ops = (lin("up", c1, x, w1, y1) + lin("down", c2, y1, w2, y2) + lin_bwd("down", c2, dy2, dy1, dw2)
                + lin_bwd("up", c1, dy1, dx, dw1))
+
+        def block_step():
+            # the same step through the layer API (W quantized on the second stream)
+            nv.nvfp4_linear_fwd(x, w1, c1, Y=y1, rht_seed=rh)
+            nv.nvfp4_linear_fwd(y1, w2, c2, Y=y2, rht_seed=rh)
+            nv.nvfp4_linear_bwd(dy2, None, c2, sr_seed=sr, rht_seed=rh, dX=dy1, dW=dw2)
+            nv.nvfp4_linear_bwd(dy1, None, c1, sr_seed=sr, rht_seed=rh, dX=dx, dW=dw1)
+
         nsteps = max(3, steps if m <= 8192 else steps // 2)
         per = _time_ops(nv, ops, flush, stream, nsteps)
-        step_ms = sum(per.values()) / nsteps
+        ops_step_ms = sum(per.values()) / nsteps
+        step_ms = _time_steps(nv, block_step, flush, stream, nsteps)
         flops = 6 * 2.0 * m * d_model * d_ffn
         gemm_ms = sum(v for k, v in per.items() if "gemm" in k) / nsteps
-        quant_ms = step_ms - gemm_ms
+        quant_ms = ops_step_ms - gemm_ms
         # algorithmic bytes of the quantize ops: amax read + encode read + codes and scales per layout
         bx, bh = m * d_model, m * d_ffn
         # X of up and down, and dY of down and up: each rowwise + RHT colwise from one amax read
@@ -668,7 +715,7 @@ def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
         gemm_tf = 6 * 2.0 * m * d_model * d_ffn / (gemm_ms * 1e-3) / 1e12
         quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
         out[str(m)] = {"ms_per_step": round(step_ms, 4), "tflops": round(flops / (step_ms * 1e-3) / 1e12, 1),
-                       "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tf, 1),
+                       "ms_per_step_ops": round(ops_step_ms, 4), "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tf, 1),
                        "gemm_frac": round(gemm_tf / fp4_peak, 4), "quant_ms": round(quant_ms, 4),
                        "quant_gbs": round(quant_gbs, 1), "quant_frac": round(quant_gbs / peaks["hbm"], 4),
                        "steps": nsteps, "gpu_launches_per_step": 22,

@@ -323,8 +323,16 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
  *         X^T -> xtq (RHT, RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
  * The context holds caller-allocated quantized buffers; every tensor's
  * rows/cols/ld_codes/scale_layout (MMA) must be filled in for the shapes
- * above, and the workspace must have nvfp4_workspace_size() bytes (16 KB,
- * for nvfp4_quantize_with_rht).  X, W, dY are bf16,
+ * above, and the workspace must have at least nvfp4_workspace_size() bytes
+ * (16 KB, for nvfp4_quantize_with_rht; device, 16-byte aligned).  With
+ * nvfp4_linear_workspace_size() bytes (24 KB) the forward quantizes W on a
+ * second stream while X is quantized on `stream`: the library's one
+ * non-blocking stream per device, forked from `stream` and joined back into
+ * it by events, so the results and their ordering are those of `stream`
+ * alone.  That stream is shared by every forward on the device (concurrent
+ * forwards on different streams may wait for one another's W), and a
+ * `stream` that is being captured into a CUDA graph gets both quantizations
+ * on itself.  X, W, dY are bf16,
  * row-major, contiguous.  Both SR quantizations of dY use sr_seed.
  * M, N, K must be multiples of 64 (16 for the blocks, 64 for the MMA K).
  * X may be NULL in nvfp4_linear_bwd when xtq already holds X^T's codes
@@ -345,6 +353,10 @@ typedef struct {
     size_t workspace_bytes;
     int32_t dw_accumulate;
 } nvfp4_linear_ctx;
+
+/* Workspace bytes with which nvfp4_linear_fwd / nvfp4_linear_fwd_rht
+ * quantize X and W on two streams (24 KB; see above). */
+size_t nvfp4_linear_workspace_size(void);
 
 nvfp4_status nvfp4_linear_fwd(const void* X, const void* W, void* Y, nvfp4_linear_ctx* ctx, nvfp4_stream_t stream);
 nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW, uint64_t sr_seed,

@@ -23,6 +23,7 @@ __all__ = [
     "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
     "nvfp4_transpose_bf16",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_set_wait_limit_ns", "nvfp4_scales_bytes", "nvfp4_workspace_size",
+    "nvfp4_linear_workspace_size",
     "nvfp4_checked_build", "nvfp4_checked_selftest",
     "empty_qtensor", "scales_as_linear",
 ]
@@ -87,6 +88,8 @@ def lib() -> ctypes.CDLL:
             L.nvfp4_scales_bytes.argtypes = [i64, i64, ctypes.c_int32]
             L.nvfp4_workspace_size.restype = ctypes.c_size_t
             L.nvfp4_workspace_size.argtypes = []
+            L.nvfp4_linear_workspace_size.restype = ctypes.c_size_t
+            L.nvfp4_linear_workspace_size.argtypes = []
             L.nvfp4_quantize.restype = st
             L.nvfp4_quantize.argtypes = [vp, st, i64, i64, i64, st, st, u64, tp, tp, vp, ctypes.c_size_t, vp]
             L.nvfp4_quantize_noalloc.restype = st
@@ -142,6 +145,10 @@ def nvfp4_scales_bytes(rows: int, cols: int, scale_layout: str = "mma") -> int:
 
 def nvfp4_workspace_size() -> int:
     return int(lib().nvfp4_workspace_size())
+
+
+def nvfp4_linear_workspace_size() -> int:
+    return int(lib().nvfp4_linear_workspace_size())
 
 
 _ws: dict = {}
@@ -377,7 +384,7 @@ class LinearContext:
     """Caller-owned quantized buffers of one NVFP4 linear layer Y = X W^T
     (X [M][K], W [N][K]); see nvfp4_linear_fwd / nvfp4_linear_bwd."""
 
-    def __init__(self, M: int, N: int, K: int, device):
+    def __init__(self, M: int, N: int, K: int, device, two_streams: bool = True):
         self.M, self.N, self.K = M, N, K
         self.xq = empty_qtensor(M, K, device)
         self.wq = empty_qtensor(N, K, device)
@@ -385,7 +392,9 @@ class LinearContext:
         self.dyq = empty_qtensor(M, N, device)
         self.dytq = empty_qtensor(N, M, device)
         self.xtq = empty_qtensor(K, M, device)
-        self.workspace = torch.empty(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
+        # the larger workspace lets the forward quantize W on a second stream
+        ws = nvfp4_linear_workspace_size() if two_streams else nvfp4_workspace_size()
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def c(self, dw_accumulate: bool = False) -> nvfp4_linear_ctx:
         return nvfp4_linear_ctx(self.M, self.N, self.K, self.xq.c(), self.wq.c(), self.wtq.c(), self.dyq.c(),

@@ -70,6 +70,43 @@ nvfp4_status device_info(DeviceInfo** out) {
     return NVFP4_OK;
 }
 
+// The forward's second stream: W's quantization runs there while X's runs on
+// the caller's stream (the two are independent until the Fprop GEMM).  One
+// non-blocking stream and two events per device, created on first use;
+// g_side_mu is held by a call from its fork record to its join wait, so the
+// events are never recorded by one call between another call's record and
+// wait.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mu;
+
+// The current device's second stream; the caller holds g_side_mu.
+nvfp4_status side_stream(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_CUDA, "device ordinal %d out of range", dev);
+    SideStream& ss = g_side[dev];
+    if (!ss.stream) {
+        SideStream n;
+        e = cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            if (n.join) cudaEventDestroy(n.join);
+            if (n.fork) cudaEventDestroy(n.fork);
+            if (n.stream) cudaStreamDestroy(n.stream);
+            return fail(NVFP4_ERR_CUDA, "second stream: %s", cudaGetErrorString(e));
+        }
+        ss = n;
+    }
+    *out = &ss;
+    return NVFP4_OK;
+}
+
 nvfp4_status check_launch(const char* what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
@@ -191,6 +228,8 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t scale_layout) {
 }
 
 size_t nvfp4_workspace_size(void) { return 2 * kSinglePassWorkspaceBytes; }
+
+size_t nvfp4_linear_workspace_size(void) { return 3 * kSinglePassWorkspaceBytes; }
 
 const char* nvfp4_last_error(void) { return g_err; }
 
@@ -511,8 +550,24 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
 }
 
 namespace {
+// X's quantization for the forward: xq (1x16 RTN) and, with_rht, X^T's RHT
+// codes in xtq from the same amax read; workspace: the first 16 KB.
+nvfp4_status linear_quantize_x(const void* X, bool with_rht, uint64_t rht_seed, nvfp4_linear_ctx* ctx,
+                               nvfp4_stream_t stream) {
+    const int64_t M = ctx->M, K = ctx->K;
+    if (with_rht)
+        // X 1x16 RTN for Fprop and X^T after the RHT along the tokens, RTN,
+        // for Wgrad: both tensor scales from one read of X
+        return nvfp4_quantize_with_rht(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xq, &ctx->xtq,
+                                       ctx->workspace, 2 * kSinglePassWorkspaceBytes, stream);
+    return nvfp4_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_BLOCK_1x16, NVFP4_RTN, 0, &ctx->xq, nullptr,
+                          ctx->workspace, kSinglePassWorkspaceBytes, stream);
+}
+
 // The forward pass; with_rht: X^T's RHT codes (xtq) as well, from the same
-// amax read of X.
+// amax read of X.  With the larger workspace, W's quantization (its own 8 KB
+// of the workspace) runs on the device's second stream, forked from and
+// joined back into `stream` by events, while X's runs on `stream`.
 nvfp4_status linear_fwd(const void* X, const void* W, void* Y, bool with_rht, uint64_t rht_seed,
                         nvfp4_linear_ctx* ctx, nvfp4_stream_t stream) {
     g_err[0] = 0;
@@ -524,20 +579,46 @@ nvfp4_status linear_fwd(const void* X, const void* W, void* Y, bool with_rht, ui
     if ((st = check_linear_tensor(&ctx->xq, M, K, "xq")) || (st = check_linear_tensor(&ctx->wq, N, K, "wq")) ||
         (st = check_linear_tensor(&ctx->wtq, K, N, "wtq")))
         return st;
-    if (with_rht) {
-        if ((st = check_linear_tensor(&ctx->xtq, K, M, "xtq"))) return st;
-        // X 1x16 RTN for Fprop and X^T after the RHT along the tokens, RTN,
-        // for Wgrad: both tensor scales from one read of X
-        if ((st = nvfp4_quantize_with_rht(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xq, &ctx->xtq,
-                                          ctx->workspace, ctx->workspace_bytes, stream)))
-            return st;
-    } else if ((st = nvfp4_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_BLOCK_1x16, NVFP4_RTN, 0, &ctx->xq, nullptr,
-                                    ctx->workspace, ctx->workspace_bytes, stream))) {
-        return st;
+    if (with_rht && (st = check_linear_tensor(&ctx->xtq, K, M, "xtq"))) return st;
+    if (!ctx->workspace || ctx->workspace_bytes < nvfp4_workspace_size())
+        return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", nvfp4_workspace_size(),
+                    ctx->workspace_bytes);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // A stream being captured into a graph keeps both quantizations (the
+    // second stream is shared by every call on the device and would join
+    // the capture).
+    // (A query that fails, e.g. on the legacy stream while another stream is
+    // captured, counts as capturing; its error is cleared.)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cap = cudaStreamCaptureStatusActive;
     }
-    if ((st = nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq,
-                             ctx->workspace, ctx->workspace_bytes, stream)))
-        return st;
+    const bool two_streams =
+        ctx->workspace_bytes >= nvfp4_linear_workspace_size() && cap == cudaStreamCaptureStatusNone;
+    void* ws_w = static_cast<uint8_t*>(ctx->workspace) + (two_streams ? 2 * kSinglePassWorkspaceBytes : 0);
+    auto quantize_w = [&](cudaStream_t ws) {
+        return nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq, ws_w,
+                              kSinglePassWorkspaceBytes, reinterpret_cast<nvfp4_stream_t>(ws));
+    };
+    if (!two_streams) {
+        if ((st = linear_quantize_x(X, with_rht, rht_seed, ctx, stream)) || (st = quantize_w(s))) return st;
+    } else {
+        std::lock_guard<std::mutex> lk(g_side_mu);
+        SideStream* side;
+        if ((st = side_stream(&side))) return st;
+        e = cudaEventRecord(side->fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "fork to the second stream: %s", cudaGetErrorString(e));
+        // whatever fails, the second stream is joined back before returning
+        st = quantize_w(side->stream);
+        if (!st) st = linear_quantize_x(X, with_rht, rht_seed, ctx, stream);
+        e = cudaEventRecord(side->join, side->stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join, 0);
+        if (st) return st;
+        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "join of the second stream: %s", cudaGetErrorString(e));
+    }
     return nvfp4_gemm(&ctx->xq, &ctx->wq, Y, NVFP4_OUT_BF16, N, nullptr, 0, stream);
 }
 }  // namespace

@@ -89,6 +89,9 @@ def test_scales_bytes(L):
     assert q.nvfp4_scales_bytes(200, 320, "mma") == 2 * 8 * 512
     assert q.nvfp4_scales_bytes(16, 17, "mma") == 0          # cols not a multiple of 16
     assert q.nvfp4_workspace_size() >= 4096
+    # the layer's workspace: nvfp4_quantize_with_rht's 16 KB plus the 8 KB
+    # of W's quantization on the second stream
+    assert q.nvfp4_linear_workspace_size() == q.nvfp4_workspace_size() * 3 // 2
 
 
 def test_host_argument_checks_need_no_gpu(L):

@@ -81,3 +81,68 @@ def test_forward_with_rht_matches_the_two_pass_layer(nv):
         assert torch.equal(qa.amax[:3], qb.amax[:3]), name      # {A, S_dec, S_enc}
     assert torch.equal(ya, yb) and torch.equal(dxa, dxb) and torch.equal(dwa, dwb)
     assert_quant_equal(b.xtq, oracle.quantize(to_f32_np(x), layout="col", rht_seed=rh), what="xtq from the forward")
+
+
+def _quantized_equal(a, b, names=("xq", "wq", "wtq", "dyq", "dytq", "xtq")):
+    for name in names:
+        qa, qb = getattr(a, name), getattr(b, name)
+        assert torch.equal(qa.codes, qb.codes) and torch.equal(qa.scales, qb.scales), name
+        assert torch.equal(qa.amax[:3], qb.amax[:3]), name
+
+
+def test_two_stream_forward_equals_one_stream(nv):
+    # With the larger workspace the forward quantizes W on the library's
+    # second stream while X is quantized on the caller's; the results must
+    # equal the one-stream forward bit for bit, repeatedly, and the caller's
+    # stream must see them without any synchronization of its own.
+    m, n, k = 512, 1024, 768
+    x, w, dy = workloads.linear_layer(m, n, k)
+    x, w, dy = x.cuda(), w.cuda(), dy.cuda()
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    one = nv.LinearContext(m, n, k, "cuda", two_streams=False)
+    two = nv.LinearContext(m, n, k, "cuda")
+    assert one.workspace.numel() == nv.nvfp4_workspace_size()
+    assert two.workspace.numel() == nv.nvfp4_linear_workspace_size()
+    y1 = nv.nvfp4_linear_fwd(x, w, one, rht_seed=rh)
+    dx1, dw1 = nv.nvfp4_linear_bwd(dy, None, one, sr_seed=sr, rht_seed=rh)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        s.wait_stream(torch.cuda.default_stream())
+        for _ in range(3):
+            y2 = nv.nvfp4_linear_fwd(x, w, two, rht_seed=rh)
+            dx2, dw2 = nv.nvfp4_linear_bwd(dy, None, two, sr_seed=sr, rht_seed=rh)
+            # read on the caller's stream right after the forward's join
+            wsum = two.wtq.codes.to(torch.int64).sum()
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    _quantized_equal(one, two)
+    assert torch.equal(y1, y2) and torch.equal(dx1, dx2) and torch.equal(dw1, dw2)
+    assert int(wsum) == int(one.wtq.codes.to(torch.int64).sum())
+
+
+def test_layer_step_captured_in_a_cuda_graph(nv):
+    # The layer's forward and backward captured into one CUDA graph and
+    # replayed: the same results as the eager calls (under capture the
+    # forward keeps both quantizations on the capturing stream).
+    m, n, k = 256, 384, 320
+    x, w, dy = workloads.linear_layer(m, n, k)
+    x, w, dy = x.cuda(), w.cuda(), dy.cuda()
+    sr, rh = workloads.SR_SEED, workloads.RHT_SEED
+    eager = nv.LinearContext(m, n, k, "cuda")
+    ye = nv.nvfp4_linear_fwd(x, w, eager, rht_seed=rh)
+    dxe, dwe = nv.nvfp4_linear_bwd(dy, None, eager, sr_seed=sr, rht_seed=rh)
+    torch.cuda.synchronize()
+    cap = nv.LinearContext(m, n, k, "cuda")
+    y = torch.empty_like(ye)
+    dx, dw = torch.empty_like(dxe), torch.empty_like(dwe)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        nv.nvfp4_linear_fwd(x, w, cap, Y=y, rht_seed=rh)
+        nv.nvfp4_linear_bwd(dy, None, cap, sr_seed=sr, rht_seed=rh, dX=dx, dW=dw)
+    for _ in range(2):
+        y.zero_(); dx.zero_(); dw.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert nv.nvfp4_sync_status() == nv.OK
+        _quantized_equal(eager, cap)
+        assert torch.equal(ye, y) and torch.equal(dxe, dx) and torch.equal(dwe, dw)
