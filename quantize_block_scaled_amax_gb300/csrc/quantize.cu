@@ -70,6 +70,34 @@ __device__ __forceinline__ uint32_t vec_absmax_bits<float>(uint4 u) {
     return max(max(u.x & 0x7FFFFFFFu, u.y & 0x7FFFFFFFu), max(u.z & 0x7FFFFFFFu, u.w & 0x7FFFFFFFu));
 }
 
+// Packed bf16 maxima of magnitudes: max(|a|, |b|) in each half, the sign
+// bit of each half the XOR of the inputs' signs (callers mask it); a NaN in
+// either input gives the canonical NaN 0x7FFF, so a block holding a NaN still
+// has a maximum pattern >= 0x7f800000 once widened.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The larger magnitude of the two halves of a packed bf16x2 magnitude word,
+// as the FP32 bit pattern of that bf16 value.
+__device__ __forceinline__ uint32_t bf16x2_widen_max(uint32_t m) {
+    return bf16x2_absmax(m, __byte_perm(m, 0u, 0x1032)) & 0x7FFF0000u;
+}
+
+// vec_absmax_bits by packed maxima (the encode passes; the amax pass keeps
+// the integer form, whose NaN patterns it reports as they are)
+template <typename T>
+__device__ __forceinline__ uint32_t vec_absmax_bits_enc(uint4 u) {
+    return vec_absmax_bits<T>(u);
+}
+
+template <>
+__device__ __forceinline__ uint32_t vec_absmax_bits_enc<__nv_bfloat16>(uint4 u) {
+    return bf16x2_widen_max(bf16x2_absmax(bf16x2_absmax(u.x, u.y), bf16x2_absmax(u.z, u.w)));
+}
+
 // element c of a 16-byte vector, as FP32
 template <typename T>
 __device__ __forceinline__ float vec_elem(const uint4& u, int c);
@@ -286,7 +314,7 @@ struct Block16 {
     __device__ __forceinline__ uint32_t absmax_bits() const {
         uint32_t m = 0;
 #pragma unroll
-        for (int k = 0; k < kVecs; ++k) m = max(m, vec_absmax_bits<T>(raw[k]));
+        for (int k = 0; k < kVecs; ++k) m = max(m, vec_absmax_bits_enc<T>(raw[k]));
         return m;
     }
     __device__ __forceinline__ void unpack(float v[16]) const {
@@ -597,11 +625,12 @@ template <>
 struct Quad<__nv_bfloat16> {
     uint2 u;
     __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint2*>(p)); }
-    // running maximum of the magnitudes, as packed 16-bit bf16 patterns
+    // running maximum of the magnitudes, packed bf16 (sign bits are
+    // don't-cares until widen)
     __device__ __forceinline__ uint32_t absmax_acc(uint32_t acc) const {
-        return __vmaxu2(__vmaxu2(acc, u.x & 0x7FFF7FFFu), u.y & 0x7FFF7FFFu);
+        return bf16x2_absmax(bf16x2_absmax(acc, u.x), u.y);
     }
-    __device__ __forceinline__ static uint32_t widen(uint32_t acc) { return max(acc & 0xFFFFu, acc >> 16) << 16; }
+    __device__ __forceinline__ static uint32_t widen(uint32_t acc) { return bf16x2_widen_max(acc); }
     __device__ __forceinline__ void pairs(uint64_t& p01, uint64_t& p23) const {
         p01 = f32x2_pack(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u));
         p23 = f32x2_pack(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
