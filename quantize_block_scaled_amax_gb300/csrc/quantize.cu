@@ -222,7 +222,14 @@ __device__ __forceinline__ uint32_t raw_absmax_acc(uint32_t acc, uint2 w);
 
 template <>
 __device__ __forceinline__ uint32_t raw_absmax_acc<__nv_bfloat16>(uint32_t acc, uint2 w) {
-    return __vmaxu2(__vmaxu2(acc, w.x & 0x7FFF7FFFu), w.y & 0x7FFF7FFFu);  // packed bf16 magnitudes
+    return bf16x2_absmax(bf16x2_absmax(acc, w.x), w.y);  // packed bf16 magnitudes (sign bits: don't-cares)
+}
+
+// max(|a|, |b|, |c|); any NaN input gives the canonical NaN
+__device__ __forceinline__ float absmax3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 template <>
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(kRhtAmaxThreads, kPlain ? 2 : 3) rht_amax_kern
     const uint32_t dmask = rht_sign_mask(rht_seed);
     const int64_t vpr = cols / V;  // column vectors per row block
     const int64_t nunits = (rows / 16) * vpr;
-    uint32_t m = 0;  // max |y| bit pattern (a NaN or an infinity gives >= 0x7f800000)
+    float my = 0.0f;  // max |y| (a NaN propagates)
     uint32_t mp = 0;  // kPlain: max |x| (packed 16-bit patterns for bf16)
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nunits;
          u += (int64_t)gridDim.x * blockDim.x) {
@@ -261,16 +268,16 @@ __global__ void __launch_bounds__(kRhtAmaxThreads, kPlain ? 2 : 3) rht_amax_kern
             rht16_pair_unscaled(v);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                m = max(m, max((uint32_t)v[i] & 0x7FFFFFFFu, (uint32_t)(v[i] >> 32) & 0x7FFFFFFFu));
+                my = absmax3_nan(my, __uint_as_float((uint32_t)v[i]), __uint_as_float((uint32_t)(v[i] >> 32)));
         }
     }
     // the maximum of fl(|y| / 4) is fl(max |y| / 4) (monotone); a NaN or an
     // infinity stays a pattern >= 0x7f800000
-    m = __float_as_uint(__fmul_rn(__uint_as_float(m), 0.25f)) & 0x7FFFFFFFu;
+    uint32_t m = __float_as_uint(__fmul_rn(my, 0.25f)) & 0x7FFFFFFFu;
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
     if constexpr (kPlain) {
-        if (sizeof(T) == 2) mp = max(mp & 0xFFFFu, mp >> 16) << 16;  // widen to an FP32 pattern
+        if (sizeof(T) == 2) mp = bf16x2_widen_max(mp);  // to an FP32 pattern
         mp = block_max_u32(mp, red);
         if (threadIdx.x == 0) partials_plain[blockIdx.x] = mp;
     }
