@@ -212,8 +212,10 @@ int cap_grid(int64_t units, int per_sm, int num_sms) {
 // CTAs of the RHT amax pass: a unit is 16 rows x one 8-byte column vector
 int rht_amax_grid(int64_t rows, int64_t cols, bool fp32, int num_sms) {
     const int64_t units = (rows / 16) * (cols / (fp32 ? 2 : 4));
+    // one wave of the kernel's 3 CTAs per SM: fewer partials for every
+    // encode CTA to reduce than with more, shorter CTAs
     return (int)std::max<int64_t>(1, std::min<int64_t>({ceil_div(units, (int64_t)kRhtAmaxThreads),
-                                                       (int64_t)num_sms * 6, (int64_t)kMaxPartials}));
+                                                       (int64_t)num_sms * 3, (int64_t)kMaxPartials}));
 }
 
 }  // namespace

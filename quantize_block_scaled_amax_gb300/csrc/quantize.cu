@@ -238,7 +238,7 @@ __device__ __forceinline__ uint32_t raw_absmax_acc<float>(uint32_t acc, uint2 w)
 }
 
 template <typename T, bool kPlain>
-__global__ void __launch_bounds__(kRhtAmaxThreads, kPlain ? 2 : 3) rht_amax_kernel(const T* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kRhtAmaxThreads, 3) rht_amax_kernel(const T* __restrict__ x, int64_t rows,
                                                                      int64_t cols, int64_t ldx, uint64_t rht_seed,
                                                                      uint32_t* __restrict__ partials,
                                                                      uint32_t* __restrict__ partials_plain) {
