@@ -398,8 +398,12 @@ __device__ __forceinline__ uint2 mx_encode16(float v[16], uint32_t bmax_bits, co
 // UE8M0 scale is written in both 16-block slots.
 // kRHT: each 16-element block is first transformed by the 16-point RHT (the
 // block is the transform's chunk), and block maxima are taken afterwards.
+// Launch bounds: 4 CTAs of 256 threads per SM (64 registers) except the RHT
+// forms with SR or FP32 input, whose transformed blocks need more registers
+// (2 CTAs; at 3 or 4 they spilled and the SR one ran 6% slower).
 template <typename T, bool kSR, bool kMX, bool kRHT>
-__global__ void __launch_bounds__(kQuantThreads, sizeof(T) == 2 ? 4 : 3) quantize_rowwise_kernel(
+__global__ void __launch_bounds__(kQuantThreads, kRHT ? ((kSR || sizeof(T) == 4) ? 2 : 4) : (sizeof(T) == 2 ? 4 : 3))
+    quantize_rowwise_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, const uint32_t* __restrict__ partials,
     int npartials, uint8_t* __restrict__ codes, int64_t ld_codes, ScaleOut so, float* amax_out, uint32_t* status,
     const __grid_constant__ PhiloxKey key, uint64_t rht_seed) {

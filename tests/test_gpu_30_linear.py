@@ -146,3 +146,51 @@ def test_layer_step_captured_in_a_cuda_graph(nv):
         assert nv.nvfp4_sync_status() == nv.OK
         _quantized_equal(eager, cap)
         assert torch.equal(ye, y) and torch.equal(dxe, dx) and torch.equal(dwe, dw)
+
+
+def test_two_stream_forwards_from_two_threads(nv):
+    # Two host threads, each with its own context and stream, run forwards
+    # at the same time: the library's second stream and its fork/join
+    # events are shared by both, so their record-to-wait sequences must not
+    # interleave.  Every result must equal the one-stream forward.
+    import threading
+    m, n, k = 256, 384, 320
+    rh = workloads.RHT_SEED
+    inputs = [(workloads.activations(m, k, seed=workloads.SEED_BASE + 40 + t),
+               workloads.weights(n, k, seed=workloads.SEED_BASE + 42 + t), None) for t in (0, 1)]
+    refs = []
+    for x, w, _ in inputs:
+        c = nv.LinearContext(m, n, k, "cuda", two_streams=False)
+        refs.append((nv.nvfp4_linear_fwd(x.cuda(), w.cuda(), c, rht_seed=rh), c))
+    torch.cuda.synchronize()
+    outs, errors = [None, None], []
+
+    def run(t):
+        try:
+            x, w, _ = inputs[t]
+            x, w = x.cuda(), w.cuda()
+            c = nv.LinearContext(m, n, k, "cuda")
+            s = torch.cuda.Stream()
+            ys = []
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    ys.append(nv.nvfp4_linear_fwd(x, w, c, rht_seed=rh))
+            s.synchronize()
+            outs[t] = (ys, c)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(t,)) for t in (0, 1)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    for t in (0, 1):
+        ys, c = outs[t]
+        y_ref, c_ref = refs[t]
+        for y in ys:
+            assert torch.equal(y, y_ref)
+        _quantized_equal(c_ref, c, names=("xq", "wq", "wtq", "xtq"))
