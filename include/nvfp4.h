@@ -284,6 +284,22 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
                         int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm_pair -- two independent nvfp4_gemm problems (C0 = A0 B0^T and
+ * C1 = A1 B1^T, each argument as nvfp4_gemm's) in one persistent launch,
+ * such as a linear layer's Dgrad and Wgrad.  A launch keeps one 256 x 256
+ * tile per SM pair at a time; a GEMM alone leaves part of the GPU idle in
+ * its last round of tiles, and here the other GEMM's tiles fill that round
+ * (the SM pairs with a tile fewer of the costlier problem take the other's
+ * tiles first).  Each output is bit for bit what nvfp4_gemm gives for it
+ * alone.  Both problems must have the same format (NVFP4 or MXFP4); C0 and
+ * C1 must not overlap each other or any operand.
+ * Errors: those of nvfp4_gemm for either problem, before any launch.
+ */
+nvfp4_status nvfp4_gemm_pair(const nvfp4_tensor* A0, const nvfp4_tensor* B0, void* C0, nvfp4_out_dtype out_dtype0,
+                             int64_t ldc0, const nvfp4_tensor* A1, const nvfp4_tensor* B1, void* C1,
+                             nvfp4_out_dtype out_dtype1, int64_t ldc1, nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm_bf16 -- C[m][n] = sum_k A[m][k] B[n][k] with bf16 A and B and
  * FP32 accumulation on the tcgen05 tensor cores (kind::f16): the GEMM of the
  * linear layers the recipe keeps in high precision (paper page, recipe
@@ -319,8 +335,9 @@ nvfp4_status nvfp4_transpose_bf16(const void* x, int64_t rows, int64_t cols, int
  *         Y[M][N] (bf16) = gemm(xq, wq).
  *   bwd:  dY -> dyq (1x16 SR) and, after the RHT along tokens with
  *         rht_seed, dY^T -> dytq (SR), both from one amax read
- *         (nvfp4_quantize_with_rht);  dX[M][K] (bf16) = gemm(dyq, wtq);
- *         X^T -> xtq (RHT, RTN);  dW[N][K] (fp32) = gemm(dytq, xtq).
+ *         (nvfp4_quantize_with_rht);  X^T -> xtq (RHT, RTN);
+ *         dX[M][K] (bf16) = gemm(dyq, wtq) and dW[N][K] (fp32) =
+ *         gemm(dytq, xtq), the two in one launch (nvfp4_gemm_pair).
  * The context holds caller-allocated quantized buffers; every tensor's
  * rows/cols/ld_codes/scale_layout (MMA) must be filled in for the shapes
  * above, and the workspace must have at least nvfp4_workspace_size() bytes

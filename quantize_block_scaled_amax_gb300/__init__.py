@@ -20,6 +20,7 @@ from . import build as _build
 
 __all__ = [
     "NVFP4Error", "QTensor", "LinearContext", "lib", "nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm",
+    "nvfp4_gemm_pair",
     "nvfp4_quantize_noalloc", "nvfp4_quantize_with_rht", "nvfp4_rht_quantize_rowwise", "nvfp4_gemm_bf16",
     "nvfp4_transpose_bf16",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_sync_status", "nvfp4_set_wait_limit_ns", "nvfp4_scales_bytes", "nvfp4_workspace_size",
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
                                                      vp]
             L.nvfp4_gemm.restype = st
             L.nvfp4_gemm.argtypes = [tp, tp, vp, st, i64, vp, ctypes.c_size_t, vp]
+            L.nvfp4_gemm_pair.restype = st
+            L.nvfp4_gemm_pair.argtypes = [tp, tp, vp, st, i64, tp, tp, vp, st, i64, vp]
             L.nvfp4_gemm_bf16.restype = st
             L.nvfp4_gemm_bf16.argtypes = [vp, i64, vp, i64, vp, st, i64, i64, i64, i64, vp]
             L.nvfp4_linear_fwd.restype = st
@@ -345,6 +348,19 @@ def nvfp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: torch.Tens
                           _stream(stream))
     _check(st, "nvfp4_gemm")
     return out
+
+
+def nvfp4_gemm_pair(a0: QTensor, b0: QTensor, out0: torch.Tensor, a1: QTensor, b1: QTensor, out1: torch.Tensor,
+                    stream=None, accumulate0: bool = False, accumulate1: bool = False):
+    """nvfp4_gemm(a0, b0, out=out0) and nvfp4_gemm(a1, b1, out=out1) in one
+    launch (bit for bit the same outputs)."""
+    od0, od1 = _out_mode(out0, accumulate0), _out_mode(out1, accumulate1)
+    c = [t.c() for t in (a0, b0, a1, b1)]
+    st = lib().nvfp4_gemm_pair(ctypes.byref(c[0]), ctypes.byref(c[1]), out0.data_ptr(), od0, out0.stride(0),
+                               ctypes.byref(c[2]), ctypes.byref(c[3]), out1.data_ptr(), od1, out1.stride(0),
+                               _stream(stream))
+    _check(st, "nvfp4_gemm_pair")
+    return out0, out1
 
 
 def nvfp4_gemm_bf16(a: torch.Tensor, b: torch.Tensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,

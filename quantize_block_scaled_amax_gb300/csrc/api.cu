@@ -433,11 +433,10 @@ nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int
     return check_launch("rht_quantize_rowwise");
 }
 
-nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,
-                        int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
-    g_err[0] = 0;
+namespace {
+// Checks one block-scaled GEMM's arguments and fills its launch arguments.
+nvfp4_status gemm_args(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype, int64_t ldc,
+                       GemmArgs* g) {
     if (!A || !B || !C) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
     nvfp4_status st;
     if ((st = check_out(A, A->rows, A->cols, "A")) || (st = check_out(B, B->rows, B->cols, "B"))) return st;
@@ -457,31 +456,60 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
         return fail(NVFP4_ERR_INVALID_ARG, "C: ldc must be >= N and 16-byte rows, C 16-byte aligned");
     DeviceInfo* dev;
     if ((st = device_info(&dev))) return st;
-    GemmArgs g;
-    g.a_codes = A->codes;
-    g.a_scales = A->scales;
-    g.a_amax = A->amax;
-    g.lda = A->ld_codes;
-    g.b_codes = B->codes;
-    g.b_scales = B->scales;
-    g.b_amax = B->amax;
-    g.ldb = B->ld_codes;
-    g.c = C;
-    g.ldc = ldc;
-    g.M = A->rows;
-    g.N = B->rows;
-    g.K = A->cols;
-    g.out_fp32 = out_dtype != NVFP4_OUT_BF16;
-    g.accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
-    g.mx = A->format == NVFP4_FORMAT_MXFP4;
-    g.timeout_ns = g_wait_limit_ns.load();
-    g.status = dev->status;
-    g.num_sms = dev->num_sms;
-    const char* msg = nullptr;
-    int e = launch_gemm(g, reinterpret_cast<cudaStream_t>(stream), &msg);
+    g->a_codes = A->codes;
+    g->a_scales = A->scales;
+    g->a_amax = A->amax;
+    g->lda = A->ld_codes;
+    g->b_codes = B->codes;
+    g->b_scales = B->scales;
+    g->b_amax = B->amax;
+    g->ldb = B->ld_codes;
+    g->c = C;
+    g->ldc = ldc;
+    g->M = A->rows;
+    g->N = B->rows;
+    g->K = A->cols;
+    g->out_fp32 = out_dtype != NVFP4_OUT_BF16;
+    g->accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
+    g->mx = A->format == NVFP4_FORMAT_MXFP4;
+    g->timeout_ns = g_wait_limit_ns.load();
+    g->status = dev->status;
+    g->num_sms = dev->num_sms;
+    return NVFP4_OK;
+}
+
+nvfp4_status gemm_launch_status(int e, const char* msg) {
     if (e == -1) return fail(NVFP4_ERR_UNSUPPORTED, "gemm: %s", msg ? msg : "unsupported");
     if (e) return fail(NVFP4_ERR_CUDA, "gemm: %s", msg ? msg : cudaGetErrorString((cudaError_t)e));
     return check_launch("gemm");
+}
+}  // namespace
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype,
+                        int64_t ldc, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    g_err[0] = 0;
+    GemmArgs g;
+    nvfp4_status st;
+    if ((st = gemm_args(A, B, C, out_dtype, ldc, &g))) return st;
+    const char* msg = nullptr;
+    const int e = launch_gemm(g, reinterpret_cast<cudaStream_t>(stream), &msg);
+    return gemm_launch_status(e, msg);
+}
+
+nvfp4_status nvfp4_gemm_pair(const nvfp4_tensor* A0, const nvfp4_tensor* B0, void* C0, nvfp4_out_dtype out_dtype0,
+                             int64_t ldc0, const nvfp4_tensor* A1, const nvfp4_tensor* B1, void* C1,
+                             nvfp4_out_dtype out_dtype1, int64_t ldc1, nvfp4_stream_t stream) {
+    g_err[0] = 0;
+    GemmArgs g0, g1;
+    nvfp4_status st;
+    if ((st = gemm_args(A0, B0, C0, out_dtype0, ldc0, &g0)) || (st = gemm_args(A1, B1, C1, out_dtype1, ldc1, &g1)))
+        return st;
+    if (g0.mx != g1.mx) return fail(NVFP4_ERR_INVALID_ARG, "the two GEMMs must share one operand format");
+    const char* msg = nullptr;
+    const int e = launch_gemm_pair(g0, g1, reinterpret_cast<cudaStream_t>(stream), &msg);
+    return gemm_launch_status(e, msg);
 }
 
 nvfp4_status nvfp4_gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
@@ -650,15 +678,15 @@ nvfp4_status nvfp4_linear_bwd(const void* dY, const void* X, void* dX, float* dW
     if ((st = nvfp4_quantize_with_rht(dY, NVFP4_IN_BF16, M, N, N, NVFP4_SR, sr_seed, rht_seed, &ctx->dyq, &ctx->dytq,
                                       ctx->workspace, ctx->workspace_bytes, stream)))
         return st;
-    // Dgrad: dX = dY W with the 16x16 weight codes of W^T
-    if ((st = nvfp4_gemm(&ctx->dyq, &ctx->wtq, dX, NVFP4_OUT_BF16, K, nullptr, 0, stream))) return st;
-    // Wgrad: dW = dY^T X with both operands transformed along the tokens
-    // (X null: xtq already holds X^T's codes from nvfp4_linear_fwd_rht)
+    // Wgrad's X operand: X^T transformed along the tokens (X null: xtq
+    // already holds X^T's codes from nvfp4_linear_fwd_rht)
     if (X && (st = nvfp4_rht_quantize(X, NVFP4_IN_BF16, M, K, K, NVFP4_RTN, 0, rht_seed, &ctx->xtq, ctx->workspace,
                                       ctx->workspace_bytes, stream)))
         return st;
-    return nvfp4_gemm(&ctx->dytq, &ctx->xtq, dW, ctx->dw_accumulate ? NVFP4_OUT_FP32_ADD : NVFP4_OUT_FP32, K, nullptr,
-                      0, stream);
+    // Dgrad dX = dY W (the 16x16 weight codes of W^T) and Wgrad dW = dY^T X
+    // (both operands transformed along the tokens) in one launch
+    return nvfp4_gemm_pair(&ctx->dyq, &ctx->wtq, dX, NVFP4_OUT_BF16, K, &ctx->dytq, &ctx->xtq, dW,
+                           ctx->dw_accumulate ? NVFP4_OUT_FP32_ADD : NVFP4_OUT_FP32, K, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -63,7 +63,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
+#include <utility>
 
 #include "nvfp4_device.cuh"
 #include "nvfp4_launch.h"
@@ -404,6 +406,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---- the kernel ----------------------------------------------------------------
+// One GEMM problem.
 struct Params {
     const uint8_t* a_scales;  // MMA layout (512-byte atoms), rows padded to 128
     const uint8_t* b_scales;
@@ -422,23 +425,59 @@ struct Params {
     uint32_t* status;
 };
 
-// Tile schedule: cluster c takes pair tiles c, c + clusters, ... of a
-// banded raster.  The M tiles are cut into bands of `group_m` rows; a band's
-// tiles come one after the other, M fastest, so the clusters running at one
-// time share a few B panels and the band's A panels, which stay in L2 while
-// the band's B panels stream past them once.  (With one band over a long-K
-// operand, say 32 A panels of 3 MB, the A panels fell out of L2 between
-// waves and were read from DRAM six times over.)
+// The kernel's parameter: one GEMM problem, or two run by one persistent
+// launch (a layer's Dgrad and Wgrad), with their operand and output maps.
+struct Maps {
+    CUtensorMap a, b, c;
+};
+struct Launch {
+    Maps maps[2];
+    Params p[2];
+    int nprob;  // 1 or 2; both problems have the same operand kind
+    int extra;  // problem-1 tiles each lightly loaded cluster takes first (see Sched)
+};
+
+// Tile schedule.  Problem 0: cluster c takes pair tiles c, c + C, ... (C
+// clusters).  Its last round leaves the clusters from r0 = T0 % C on with one
+// tile fewer; with two problems each of those first takes `extra` tiles of
+// problem 1 (about one problem-0 tile's worth of work), and the rest of
+// problem 1 is dealt round robin, so the two problems' tails even out across
+// the clusters.  Within a problem the tiles follow a banded raster: the M
+// tiles are cut into bands of `group_m` rows and a band's tiles come one
+// after the other, M fastest, so the clusters running at one time share a
+// few B panels and the band's A panels, which stay in L2 while the band's B
+// panels stream past them once.  (With one band over a long-K operand, say
+// 32 A panels of 3 MB, the A panels fell out of L2 between waves and were
+// read from DRAM six times over.)
 struct Sched {
-    int num_tiles, cid, nclusters;
-    __device__ explicit Sched(const Params& p) {
-        num_tiles = p.num_m * p.num_n;
+    int cid, C, r0, e, E, n0, nex, nrr;
+    __device__ explicit Sched(const Launch& L) {
         cid = (int)blockIdx.x >> 1;
-        nclusters = (int)gridDim.x >> 1;
+        C = (int)gridDim.x >> 1;
+        const int t0 = L.p[0].num_m * L.p[0].num_n;
+        const int t1 = L.nprob > 1 ? L.p[1].num_m * L.p[1].num_n : 0;
+        r0 = t0 % C;
+        e = (t1 > 0 && r0 > 0) ? L.extra : 0;
+        E = min(t1, (C - r0) * e);
+        n0 = cid < t0 ? (t0 - cid + C - 1) / C : 0;
+        nex = (e > 0 && cid >= r0) ? max(0, min(e, E - (cid - r0) * e)) : 0;
+        nrr = cid < t1 - E ? (t1 - E - cid + C - 1) / C : 0;
     }
-    __device__ int count() const { return cid < num_tiles ? (num_tiles - cid + nclusters - 1) / nclusters : 0; }
-    __device__ void tile(int i, const Params& p, int& mt, int& nt) const {
-        const int t = cid + i * nclusters;
+    __device__ int count() const { return n0 + nex + nrr; }
+    // problem g and pair tile (mt, nt) of this cluster's i-th tile
+    __device__ void tile(int i, const Launch& L, int& g, int& mt, int& nt) const {
+        int t;
+        if (i < n0) {
+            g = 0;
+            t = cid + i * C;
+        } else if (i < n0 + nex) {
+            g = 1;
+            t = (cid - r0) * e + (i - n0);
+        } else {
+            g = 1;
+            t = E + cid + (i - n0 - nex) * C;
+        }
+        const Params& p = L.p[g];
         const int band_tiles = p.group_m * p.num_n;
         const int band = t / band_tiles;
         const int m0 = band * p.group_m;
@@ -452,15 +491,17 @@ struct Sched {
 // Code producer (one lane, both CTAs): this CTA's A rows and B rows of each
 // stage, counted on the leader's `full` barrier.  A stage is refilled once
 // the MMAs that read it have completed (`empty`, committed to both CTAs).
-__device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
-                                              SharedState* ss, uint8_t* stages, uint32_t rank) {
-    const Sched S(p);
+__device__ __forceinline__ void producer_role(const Launch& L, SharedState* ss, uint8_t* stages, uint32_t rank) {
+    const Sched S(L);
     // the leader's `full` barriers (consecutive words of its shared window)
     const uint32_t full_l0 = leader_addr(&ss->full[0]);
     uint32_t it = 0;
     for (int i = 0; i < S.count(); ++i) {
-        int mt, nt;
-        S.tile(i, p, mt, nt);
+        int g, mt, nt;
+        S.tile(i, L, g, mt, nt);
+        const Params& p = L.p[g];
+        const CUtensorMap* tmap_a = &L.maps[g].a;
+        const CUtensorMap* tmap_b = &L.maps[g].b;
         const int ya = mt * kPairM + (int)rank * BM;
         const int yb = nt * BN + (int)rank * kBRows;
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
@@ -482,13 +523,14 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmap_a, const C
 // Scale producer (one lane, both CTAs, NVFP4/MXFP4 only): the stage's scale
 // atoms, its A rows' 2 KB run and both B groups' runs, into the stage buffer,
 // counted on this CTA's `sf_in` barrier.
-__device__ __forceinline__ void scale_producer_role(const Params& p, SharedState* ss, uint8_t* stages,
+__device__ __forceinline__ void scale_producer_role(const Launch& L, SharedState* ss, uint8_t* stages,
                                                     uint32_t rank) {
-    const Sched S(p);
+    const Sched S(L);
     uint32_t it = 0;
     for (int i = 0; i < S.count(); ++i) {
-        int mt, nt;
-        S.tile(i, p, mt, nt);
+        int g, mt, nt;
+        S.tile(i, L, g, mt, nt);
+        const Params& p = L.p[g];
         const int ga = 2 * mt + (int)rank;                // this CTA's A group
         const bool a_in = ga < p.a_groups;
         const int nb = min(2, p.b_groups - 2 * nt);       // B groups of the pair tile that exist
@@ -526,8 +568,9 @@ enum MmaKind { kNvf4 = 0, kMxf4 = 1, kBf16 = 2 };
 // MMAs of a stage keep the tensor pipe busy for 512 cycles; everything this
 // thread does per stage has to fit in that.  Returns false on abort.
 template <int kKind>
-__device__ __forceinline__ bool mma_loop(const Params& p, SharedState* ss, uint8_t* stages, uint32_t tmem_base) {
-    const Sched S(p);
+__device__ __forceinline__ bool mma_loop(const Launch& L, SharedState* ss, uint8_t* stages, uint32_t tmem_base) {
+    const Sched S(L);
+    const Params& p0 = L.p[0];  // operand kind, status and wait bound: the same in both problems
     const uint32_t idesc = kKind == kBf16 ? instr_desc_bf16(kPairM, BN) : instr_desc_nvf4(kPairM, BN, kKind == kMxf4);
     // descriptors of stage 0's tiles; stage s adds s * kStageBytes >> 4 to the
     // start-address field, MMA j adds 32 j >> 4
@@ -536,10 +579,13 @@ __device__ __forceinline__ bool mma_loop(const Params& p, SharedState* ss, uint8
     int s = 0;            // ring stage of the next MMAs, and its phase parity
     uint32_t ph = 0;
     for (int i = 0; i < S.count(); ++i) {
-        if (!mbar_wait(&ss->acc_empty, ((uint32_t)i & 1u) ^ 1u, ss, p.status, p.timeout_ns)) return false;
+        int g, mt, nt;
+        S.tile(i, L, g, mt, nt);
+        const int num_k = L.p[g].num_k;
+        if (!mbar_wait(&ss->acc_empty, ((uint32_t)i & 1u) ^ 1u, ss, p0.status, p0.timeout_ns)) return false;
         tc_fence_after();
-        for (int kt = 0; kt < p.num_k; ++kt) {
-            if (!mbar_wait(&ss->full[s], ph, ss, p.status, p.timeout_ns)) return false;
+        for (int kt = 0; kt < num_k; ++kt) {
+            if (!mbar_wait(&ss->full[s], ph, ss, p0.status, p0.timeout_ns)) return false;
             tc_fence_after();
             const uint64_t soff = (uint64_t)((uint32_t)(s * kStageBytes) >> 4);
             const uint32_t sf = tmem_base + kAccCols + (uint32_t)s * kSfColsPerSlot;
@@ -569,10 +615,10 @@ __device__ __forceinline__ bool mma_loop(const Params& p, SharedState* ss, uint8
 // Runs the MMA loop, then waits (bounded) until every MMA it issued has
 // completed, on the normal path and after an abort alike, so TMEM and the
 // stages are never released under running MMAs.
-__device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8_t* stages, uint32_t tmem_base) {
-    if (p.bf16) mma_loop<kBf16>(p, ss, stages, tmem_base);
-    else if (p.mx) mma_loop<kMxf4>(p, ss, stages, tmem_base);
-    else mma_loop<kNvf4>(p, ss, stages, tmem_base);
+__device__ __forceinline__ void mma_role(const Launch& L, SharedState* ss, uint8_t* stages, uint32_t tmem_base) {
+    if (L.p[0].bf16) mma_loop<kBf16>(L, ss, stages, tmem_base);
+    else if (L.p[0].mx) mma_loop<kMxf4>(L, ss, stages, tmem_base);
+    else mma_loop<kNvf4>(L, ss, stages, tmem_base);
     mma_commit_pair(&ss->drain);
     // MMAs finish in microseconds; the bound only guards against a fault
     const uint64_t t0 = globaltimer();
@@ -591,16 +637,17 @@ __device__ __forceinline__ void mma_role(const Params& p, SharedState* ss, uint8
 // the MMAs of the stage's previous round have completed: the scale producer
 // waited for exactly that (`empty`) before the copies that complete `sf_in`,
 // so the writers need no wait of their own for it.
-__device__ __forceinline__ void scale_role(const Params& p, SharedState* ss, const uint8_t* stages,
+__device__ __forceinline__ void scale_role(const Launch& L, SharedState* ss, const uint8_t* stages,
                                            uint32_t tmem_base, int q, int lane, uint32_t rank) {
-    const Sched S(p);
+    const Sched S(L);
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     // the leader's `full` barriers (consecutive words of its shared window)
     const uint32_t full_l0 = leader_addr(&ss->full[0]);
     uint32_t it = 0;
     for (int i = 0; i < S.count(); ++i) {
-        int mt, nt;
-        S.tile(i, p, mt, nt);
+        int g, mt, nt;
+        S.tile(i, L, g, mt, nt);
+        const Params& p = L.p[g];
         const bool a_in = 2 * mt + (int)rank < p.a_groups;
         const int nb = min(2, p.b_groups - 2 * nt);
         for (int kt = 0; kt < p.num_k; ++kt, ++it) {
@@ -711,11 +758,15 @@ __device__ __forceinline__ void stage_f32(const uint32_t* a, float alpha, uint8_
 // it), then the last 64 are loaded and the accumulator is released at once;
 // their conversion, staging and stores overlap the next tile's MMAs.  At
 // most 64 accumulator words are live per thread, so nothing is spilled.
-__device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const Params& p, SharedState* ss,
-                                              uint8_t* staging, uint32_t tmem_base, int q, int h, int lane,
-                                              uint32_t rank) {
-    const Sched S(p);
-    const float alpha = p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
+__device__ __forceinline__ void epilogue_role(const Launch& L, SharedState* ss, uint8_t* staging, uint32_t tmem_base,
+                                              int q, int h, int lane, uint32_t rank) {
+    const Sched S(L);
+    // each problem's S_dec,A * S_dec,B
+    auto alpha_of = [&](const Params& p) {
+        return p.bf16 ? 1.0f : __fmul_rn(__ldg(p.a_amax + 1), __ldg(p.b_amax + 1));
+    };
+    const float alpha0 = alpha_of(L.p[0]);
+    const float alpha1 = L.nprob > 1 ? alpha_of(L.p[1]) : 1.0f;
     const uint32_t t_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
     const uint32_t acc_empty_l = leader_addr(&ss->acc_empty);
     auto release = [&]() {
@@ -727,8 +778,11 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
         }
     };
     for (int i = 0; i < S.count(); ++i) {
-        int mt, nt;
-        S.tile(i, p, mt, nt);
+        int g, mt, nt;
+        S.tile(i, L, g, mt, nt);
+        const Params& p = L.p[g];
+        const CUtensorMap* tmap_c = &L.maps[g].c;
+        const float alpha = g ? alpha1 : alpha0;
         if (!warp_wait(&ss->acc_full, (uint32_t)i & 1u, ss, p.status, p.timeout_ns, lane)) break;
         tc_fence_after();
         const int y = mt * kPairM + (int)rank * BM + 32 * q;
@@ -787,9 +841,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmap_c, const P
     __syncwarp();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_c, const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) nvf4_gemm_kernel(const __grid_constant__ Launch L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
@@ -803,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             // both CTAs' code producers, and both CTAs' scale writers
-            mbar_init(&ss->full[s], p.bf16 ? 2 : 2 + 2 * kSfWarps);
+            mbar_init(&ss->full[s], L.p[0].bf16 ? 2 : 2 + 2 * kSfWarps);
             mbar_init(&ss->sf_in[s], 1);
             mbar_init(&ss->empty[s], 1);              // one commit per stage
         }
@@ -812,9 +864,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ss->drain, 1);
         ss->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_c) : "memory");
+        for (int g = 0; g < L.nprob; ++g) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&L.maps[g].a) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&L.maps[g].b) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&L.maps[g].c) : "memory");
+        }
     }
     if (warp == 1) {  // the pair allocates together: the same columns in both SMs
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -828,18 +882,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = ss->tmem_base;
 
+    const bool bf16 = L.p[0].bf16 != 0;
     if (warp == 0) {
-        if (lane == 0) producer_role(&tmap_a, &tmap_b, p, ss, stages, rank);
+        if (lane == 0) producer_role(L, ss, stages, rank);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) mma_role(p, ss, stages, tmem_base);
+        if (lane == 0 && rank == 0) mma_role(L, ss, stages, tmem_base);
     } else if (warp == 2) {
-        if (lane == 0 && !p.bf16) scale_producer_role(p, ss, stages, rank);
+        if (lane == 0 && !bf16) scale_producer_role(L, ss, stages, rank);
     } else if (warp >= 4 && warp < 8) {
-        if (!p.bf16) scale_role(p, ss, stages, tmem_base, warp & 3, lane, rank);
+        if (!bf16) scale_role(L, ss, stages, tmem_base, warp & 3, lane, rank);
     } else if (warp >= 8) {
         const int e = warp - 8;
-        epilogue_role(&tmap_c, p, ss, staging + e * kStagingBufs * kStagingBytes, tmem_base, warp & 3, e >> 2, lane,
-                      rank);
+        epilogue_role(L, ss, staging + e * kStagingBufs * kStagingBytes, tmem_base, warp & 3, e >> 2, lane, rank);
     }
 
     // Drain.  The MMA issuer has already waited for its MMAs.  Past the first
@@ -948,12 +1002,12 @@ int device_launch(int* clusters, const char** msg) {
     return 0;
 }
 
-int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm, const Params& p, cudaStream_t s,
-           const char** msg) {
+int launch(const Launch& L, cudaStream_t s, const char** msg) {
     int clusters = 0;
     int e = device_launch(&clusters, msg);
     if (e) return e;
-    const int64_t tiles = (int64_t)p.num_m * p.num_n;
+    int64_t tiles = 0;
+    for (int g = 0; g < L.nprob; ++g) tiles += (int64_t)L.p[g].num_m * L.p[g].num_n;
     const int64_t grid_clusters = tiles < clusters ? tiles : clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * grid_clusters));
@@ -967,7 +1021,7 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel, ta, tb, tcm, p);
+    return (int)cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel, L);
 }
 
 // M tiles per band of the raster (see Sched): as many as keep the band's A
@@ -992,19 +1046,21 @@ int make_c_map(CUtensorMap* tcm, const void* c, int64_t M, int64_t N, int64_t ld
 
 }  // namespace gemm
 
-int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
-    using namespace gemm;
-    if (get_encoder(msg)) return 1;
+namespace gemm {
+namespace {
+
+// One block-scaled problem's maps and parameters.
+int fp4_problem(const GemmArgs& g, Maps* m, Params* pp, const char** msg) {
     if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) {
         *msg = "dimension exceeds 2^31";
         return -1;
     }
-    CUtensorMap ta, tb, tcm;
-    if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.M, g.K / 2, g.lda, BKB, BM, msg) ||
-        make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, kBRows, msg) ||
-        make_c_map(&tcm, g.c, g.M, g.N, g.ldc, g.out_fp32 != 0, msg))
+    if (make_map(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.M, g.K / 2, g.lda, BKB, BM, msg) ||
+        make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.N, g.K / 2, g.ldb, BKB, kBRows, msg) ||
+        make_c_map(&m->c, g.c, g.M, g.N, g.ldc, g.out_fp32 != 0, msg))
         return 1;
-    Params p = {};
+    Params& p = *pp;
+    p = {};
     p.a_scales = g.a_scales;
     p.b_scales = g.b_scales;
     p.a_amax = g.a_amax;
@@ -1025,7 +1081,45 @@ int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
     p.bf16 = 0;
     p.timeout_ns = g.timeout_ns ? g.timeout_ns : kDefaultTimeoutNs;
     p.status = g.status;
-    return launch(ta, tb, tcm, p, s, msg);
+    return 0;
+}
+
+// Relative cost of one pair tile: its K stages plus the epilogue's share
+// (about 6 stages' time for bf16 output, 8 for FP32).
+double tile_cost(const Params& p) { return (double)p.num_k + (p.out_fp32 ? 8.0 : 6.0); }
+
+}  // namespace
+}  // namespace gemm
+
+int launch_gemm(const GemmArgs& g, cudaStream_t s, const char** msg) {
+    using namespace gemm;
+    if (get_encoder(msg)) return 1;
+    Launch L = {};
+    L.nprob = 1;
+    if (int e = fp4_problem(g, &L.maps[0], &L.p[0], msg)) return e;
+    return launch(L, s, msg);
+}
+
+int launch_gemm_pair(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s, const char** msg) {
+    using namespace gemm;
+    if (get_encoder(msg)) return 1;
+    if (g0.mx != g1.mx) {
+        *msg = "the two problems of one launch must have the same operand format";
+        return -1;
+    }
+    Launch L = {};
+    L.nprob = 2;
+    if (int e = fp4_problem(g0, &L.maps[0], &L.p[0], msg)) return e;
+    if (int e = fp4_problem(g1, &L.maps[1], &L.p[1], msg)) return e;
+    // problem 0 is the one with the costlier tiles: the clusters its last
+    // round leaves idle take the cheaper tiles of the other first
+    if (tile_cost(L.p[1]) > tile_cost(L.p[0])) {
+        std::swap(L.maps[0], L.maps[1]);
+        std::swap(L.p[0], L.p[1]);
+    }
+    const double ratio = tile_cost(L.p[0]) / tile_cost(L.p[1]);
+    L.extra = (int)std::min(8.0, std::max(0.0, ratio + 0.5));
+    return launch(L, s, msg);
 }
 
 int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
@@ -1035,12 +1129,13 @@ int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
         *msg = "dimension exceeds 2^31";
         return -1;
     }
-    CUtensorMap ta, tb, tcm;
-    if (make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, g.M, g.K, g.lda * 2, 64, BM, msg) ||
-        make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.b, g.N, g.K, g.ldb * 2, 64, kBRows, msg) ||
-        make_c_map(&tcm, g.c, g.M, g.N, g.ldc, g.out_fp32 != 0, msg))
+    Launch L = {};
+    L.nprob = 1;
+    if (make_map(&L.maps[0].a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, g.M, g.K, g.lda * 2, 64, BM, msg) ||
+        make_map(&L.maps[0].b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.b, g.N, g.K, g.ldb * 2, 64, kBRows, msg) ||
+        make_c_map(&L.maps[0].c, g.c, g.M, g.N, g.ldc, g.out_fp32 != 0, msg))
         return 1;
-    Params p = {};
+    Params& p = L.p[0];
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
@@ -1055,7 +1150,7 @@ int launch_gemm_bf16(const GemmBf16Args& g, cudaStream_t s, const char** msg) {
     p.bf16 = 1;
     p.timeout_ns = g.timeout_ns ? g.timeout_ns : kDefaultTimeoutNs;
     p.status = g.status;
-    return launch(ta, tb, tcm, p, s, msg);
+    return launch(L, s, msg);
 }
 
 }  // namespace nvfp4

@@ -67,6 +67,10 @@ struct GemmArgs {
 
 // Returns a cudaError_t-like code (0 ok) and fills `msg` on failure.
 int launch_gemm(const GemmArgs& args, cudaStream_t s, const char** msg);
+// Two block-scaled GEMMs (the same operand format) in one persistent launch,
+// their tiles dealt so that the tail of one fills the other's idle clusters;
+// each output is bit for bit what launch_gemm gives for it alone.
+int launch_gemm_pair(const GemmArgs& a, const GemmArgs& b, cudaStream_t s, const char** msg);
 
 // BF16 GEMM C = A B^T (gemm.cu, the same kernel with kind::f16 MMAs).
 struct GemmBf16Args {
