@@ -397,7 +397,10 @@ def gpu_bench(args):
         "roofline_gemm": roof_gemm,
         "kernels": kernels,
         "share": {"gemm": round(gemm_ms / (gemm_ms + quant_ms), 4), "quantize": round(quant_ms / (gemm_ms + quant_ms), 4)},
-        "gpu_launches": args.steps * sum(launches_per_op.values()),
+        # the timed steps: the op list's launches, Dgrad and Wgrad being one
+        # launch in nvfp4_linear_bwd (nvfp4_gemm_pair)
+        "gpu_launches": args.steps * (sum(launches_per_op.values()) - 1),
+        "gpu_launches_per_step_ops": sum(launches_per_op.values()),
         "mxfp4": mx,
         "rht_fprop_dgrad_quantize": rht_rows,
         "bf16_fallback_gemm": bf16_gemm,
@@ -718,7 +721,7 @@ def ffn_measure(nv, flush, stream, steps, peaks, ms=(2048, 8192, 32768)):
                        "ms_per_step_ops": round(ops_step_ms, 4), "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tf, 1),
                        "gemm_frac": round(gemm_tf / fp4_peak, 4), "quant_ms": round(quant_ms, 4),
                        "quant_gbs": round(quant_gbs, 1), "quant_frac": round(quant_gbs / peaks["hbm"], 4),
-                       "steps": nsteps, "gpu_launches_per_step": 22,
+                       "steps": nsteps, "gpu_launches_per_step": 20, "gpu_launches_per_step_ops": 22,
                        "ops_ms": {k: round(v / nsteps, 4) for k, v in per.items()}}
         del x, w1, w2, dy2, c1, c2, y1, y2, dy1, dx, dw1, dw2, ops
         torch.cuda.empty_cache()

@@ -434,7 +434,8 @@ nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int
 }
 
 namespace {
-// Checks one block-scaled GEMM's arguments and fills its launch arguments.
+// Checks one block-scaled GEMM's arguments (host only) and fills its launch
+// arguments but the device's (gemm_device).
 nvfp4_status gemm_args(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nvfp4_out_dtype out_dtype, int64_t ldc,
                        GemmArgs* g) {
     if (!A || !B || !C) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
@@ -454,8 +455,6 @@ nvfp4_status gemm_args(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nv
     const int esz = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     if (ldc < B->rows || (ldc * esz) % 16 || !aligned16(C))
         return fail(NVFP4_ERR_INVALID_ARG, "C: ldc must be >= N and 16-byte rows, C 16-byte aligned");
-    DeviceInfo* dev;
-    if ((st = device_info(&dev))) return st;
     g->a_codes = A->codes;
     g->a_scales = A->scales;
     g->a_amax = A->amax;
@@ -473,6 +472,14 @@ nvfp4_status gemm_args(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, nv
     g->accumulate = out_dtype == NVFP4_OUT_FP32_ADD;
     g->mx = A->format == NVFP4_FORMAT_MXFP4;
     g->timeout_ns = g_wait_limit_ns.load();
+    return NVFP4_OK;
+}
+
+// The current device's part of a GEMM's launch arguments.
+nvfp4_status gemm_device(GemmArgs* g) {
+    DeviceInfo* dev;
+    nvfp4_status st;
+    if ((st = device_info(&dev))) return st;
     g->status = dev->status;
     g->num_sms = dev->num_sms;
     return NVFP4_OK;
@@ -492,7 +499,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* C, n
     g_err[0] = 0;
     GemmArgs g;
     nvfp4_status st;
-    if ((st = gemm_args(A, B, C, out_dtype, ldc, &g))) return st;
+    if ((st = gemm_args(A, B, C, out_dtype, ldc, &g)) || (st = gemm_device(&g))) return st;
     const char* msg = nullptr;
     const int e = launch_gemm(g, reinterpret_cast<cudaStream_t>(stream), &msg);
     return gemm_launch_status(e, msg);
@@ -507,6 +514,7 @@ nvfp4_status nvfp4_gemm_pair(const nvfp4_tensor* A0, const nvfp4_tensor* B0, voi
     if ((st = gemm_args(A0, B0, C0, out_dtype0, ldc0, &g0)) || (st = gemm_args(A1, B1, C1, out_dtype1, ldc1, &g1)))
         return st;
     if (g0.mx != g1.mx) return fail(NVFP4_ERR_INVALID_ARG, "the two GEMMs must share one operand format");
+    if ((st = gemm_device(&g0)) || (st = gemm_device(&g1))) return st;
     const char* msg = nullptr;
     const int e = launch_gemm_pair(g0, g1, reinterpret_cast<cudaStream_t>(stream), &msg);
     return gemm_launch_status(e, msg);

@@ -190,6 +190,25 @@ def test_gemm_argument_checks_need_no_gpu(L):
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 0, 64, None, 0, None) == q.ERR_INVALID_ARG
 
 
+def test_gemm_pair_argument_checks_need_no_gpu(L):
+    # nvfp4_gemm_pair checks both problems (the same checks as nvfp4_gemm)
+    # and refuses two formats, all before any launch
+    import quantize_block_scaled_amax_gb300 as q
+    a = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 1, 0)
+    b = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 1, 0)
+    bad = q.nvfp4_tensor(16, 16, 16, 64, 64, 32, 1, 0)     # K mismatch with a
+    pair = lambda a0, b0, c0, a1, b1, c1: L.nvfp4_gemm_pair(ctypes.byref(a0), ctypes.byref(b0), c0, 0, 64,
+                                                             ctypes.byref(a1), ctypes.byref(b1), c1, 0, 64, None)
+    assert pair(a, bad, 16, a, b, 16) == q.ERR_INVALID_ARG      # first problem invalid
+    assert pair(a, b, 16, a, bad, 16) == q.ERR_INVALID_ARG      # second problem invalid
+    assert pair(a, b, None, a, b, 16) == q.ERR_INVALID_ARG      # null C0
+    assert pair(a, b, 16, a, b, 24) == q.ERR_INVALID_ARG        # C1 not 16-byte aligned
+    am = q.nvfp4_tensor(16, 16, 16, 128, 128, 64, 1, 1)
+    bm = q.nvfp4_tensor(16, 16, 16, 64, 128, 64, 1, 1)
+    assert pair(a, b, 16, am, bm, 16) == q.ERR_INVALID_ARG      # NVFP4 with MXFP4
+    assert b"format" in L.nvfp4_last_error()
+
+
 def test_rht_quantize_rowwise_argument_checks_need_no_gpu(L):
     import quantize_block_scaled_amax_gb300 as q
     t = q.nvfp4_tensor(16, 16, 16, 16, 64, 32, 1, 0)       # y [16][64], NVFP4
