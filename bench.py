@@ -788,7 +788,22 @@ def profile_case(args):
     m, n, k = args.m or M, args.n or N, args.k or K
     dev = torch.device("cuda", 0)
     op = args.profile
-    if op.startswith("gemm"):
+    if op == "gemm_pair":
+        # the layer backward's Dgrad (dY 8192x20480 by W^T 5120x20480, bf16
+        # out) and Wgrad (dY^T 20480x8192 by X^T 5120x8192, FP32 out) in one
+        # launch, on operands of those shapes
+        qs = []
+        for r, c, seed in ((M, N, 31), (K, N, 32), (N, M, 33), (K, M, 34)):
+            t = workloads.normal_with_outliers(r, c, p=0.001, factor=20.0, seed=workloads.SEED_BASE + seed,
+                                               device=dev)
+            qs.append(nv.nvfp4_quantize(t)[0])
+            del t
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        nv.nvfp4_gemm_pair(qs[0], qs[1], dx, qs[2], qs[3], dw)
+    elif op.startswith("gemm"):
         x = workloads.activations(m, k, device=dev)
         w = workloads.weights(n, k, device=dev)
         qx, _ = nv.nvfp4_quantize(x)
