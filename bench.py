@@ -855,7 +855,8 @@ def main():
     ap.add_argument("--cpu-sample-m", type=int, default=512)
     ap.add_argument("--cpu-sample-n", type=int, default=4096)
     ap.add_argument("--profile", default=None,
-                    help="run one launch of one op: gemm_fprop, quant_x_rtn, quant_w_2d, quant_dy_sr, rht_dy_sr")
+                    help="run one launch of one op: gemm_fprop, gemm, gemm_fp32, gemm_pair, quant_x_rtn, quant_w_2d, "
+                         "quant_dy_sr, rht_dy_sr")
     ap.add_argument("--m", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)
     ap.add_argument("--k", type=int, default=0)
