@@ -236,6 +236,11 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_in_dtype dtype, int64_t row
  *   workspace    device, >= 2 * 8 KB (nvfp4_workspace_size()), 16-byte
  *                aligned; NVFP4_ERR_WORKSPACE if smaller.
  *   Other arguments as nvfp4_quantize.
+ * With SR the rowwise encode runs on the library's second stream of the
+ * device (see the linear layer below), forked from `stream` after the amax
+ * pass and joined back before the call's work ends, so ordering is that of
+ * `stream` alone; a `stream` being captured into a CUDA graph keeps both
+ * encodes on itself.
  */
 nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
                                      nvfp4_round round, uint64_t seed, uint64_t rht_seed,

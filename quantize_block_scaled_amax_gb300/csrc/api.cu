@@ -70,18 +70,20 @@ nvfp4_status device_info(DeviceInfo** out) {
     return NVFP4_OK;
 }
 
-// The forward's second stream: W's quantization runs there while X's runs on
-// the caller's stream (the two are independent until the Fprop GEMM).  One
-// non-blocking stream and two events per device, created on first use;
-// g_side_mu is held by a call from its fork record to its join wait, so the
-// events are never recorded by one call between another call's record and
-// wait.
+// The second stream: independent work of one call runs there beside the
+// caller's stream (W's quantization beside X's in the forward; dY's rowwise
+// SR encode beside its colwise one).  One non-blocking stream and two events
+// per device, created on first use; g_side_mu is held by a call from its fork
+// record to its join wait, so the events are never recorded by one call
+// between another call's record and wait (recursive: a call inside a fork may
+// fork again, its work then queued behind the outer call's on the second
+// stream).
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 SideStream g_side[kMaxDevices];
-std::mutex g_side_mu;
+std::recursive_mutex g_side_mu;
 
 // The current device's second stream; the caller holds g_side_mu.
 nvfp4_status side_stream(SideStream** out) {
@@ -104,6 +106,41 @@ nvfp4_status side_stream(SideStream** out) {
         ss = n;
     }
     *out = &ss;
+    return NVFP4_OK;
+}
+
+// Runs side_work(stream) and main_work() concurrently: side_work on the
+// device's second stream, forked from `s` and joined back into it by events,
+// main_work on `s`; results and their ordering are those of `s` alone.  When
+// `allowed` is false, or `s` is being captured into a CUDA graph (the shared
+// second stream would join the capture; a query that fails, e.g. on the
+// legacy stream while another stream is captured, counts as capturing and
+// its error is cleared), both run on `s`, side_work first.  Returns the first
+// failure; the second stream is joined back whatever fails.
+template <class SideFn, class MainFn>
+nvfp4_status fork_join(cudaStream_t s, bool allowed, SideFn side_work, MainFn main_work) {
+    if (allowed) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            cap = cudaStreamCaptureStatusActive;
+        }
+        allowed = cap == cudaStreamCaptureStatusNone;
+    }
+    nvfp4_status st;
+    if (!allowed) return (st = side_work(s)) ? st : main_work();
+    std::lock_guard<std::recursive_mutex> lk(g_side_mu);
+    SideStream* side;
+    if ((st = side_stream(&side))) return st;
+    cudaError_t e = cudaEventRecord(side->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "fork to the second stream: %s", cudaGetErrorString(e));
+    st = side_work(side->stream);
+    if (!st) st = main_work();
+    e = cudaEventRecord(side->join, side->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join, 0);
+    if (st) return st;
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "join of the second stream: %s", cudaGetErrorString(e));
     return NVFP4_OK;
 }
 
@@ -387,14 +424,23 @@ nvfp4_status nvfp4_quantize_with_rht(const void* x, nvfp4_in_dtype dtype, int64_
     if ((st = check_launch("rht_amax"))) return st;
     const int64_t items = rows * ceil_div(cols / 16, (int64_t)kRowItemBlocks);
     const int gr = cap_grid(ceil_div(items, (int64_t)kQuantThreads / 32), row_ctas_per_sm(sr), dev->num_sms);
-    launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials_plain, ag, out_rowwise->codes, out_rowwise->ld_codes,
-                            scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr, false, seed, false, 0, gr, s);
-    if ((st = check_launch("quantize_rowwise"))) return st;
     const int gc = cap_grid(colwise_tiles(rows, cols), 12, dev->num_sms);
-    launch_quantize_colwise(x, fp32, rows, cols, ldx, partials_rht, ag, out_colwise->codes, out_colwise->ld_codes,
-                            scale_out(*out_colwise), out_colwise->amax, dev->status, sr, false, seed, true, rht_seed,
-                            gc, s);
-    return check_launch("rht_quantize_colwise");
+    // SR: the two encodes are issue-bound; on two streams each fills the
+    // other's tail (dY 8192x20480: 0.411 -> 0.394 ms)
+    return fork_join(
+        s, sr,
+        [&](cudaStream_t rs) {
+            launch_quantize_rowwise(x, fp32, rows, cols, ldx, partials_plain, ag, out_rowwise->codes,
+                                    out_rowwise->ld_codes, scale_out(*out_rowwise), out_rowwise->amax, dev->status, sr,
+                                    false, seed, false, 0, gr, rs);
+            return check_launch("quantize_rowwise");
+        },
+        [&]() {
+            launch_quantize_colwise(x, fp32, rows, cols, ldx, partials_rht, ag, out_colwise->codes,
+                                    out_colwise->ld_codes, scale_out(*out_colwise), out_colwise->amax, dev->status, sr,
+                                    false, seed, true, rht_seed, gc, s);
+            return check_launch("rht_quantize_colwise");
+        });
 }
 
 nvfp4_status nvfp4_rht_quantize_rowwise(const void* x, nvfp4_in_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
@@ -622,41 +668,17 @@ nvfp4_status linear_fwd(const void* X, const void* W, void* Y, bool with_rht, ui
         return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", nvfp4_workspace_size(),
                     ctx->workspace_bytes);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // A stream being captured into a graph keeps both quantizations (the
-    // second stream is shared by every call on the device and would join
-    // the capture).
-    // (A query that fails, e.g. on the legacy stream while another stream is
-    // captured, counts as capturing; its error is cleared.)
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    cudaError_t e = cudaStreamIsCapturing(s, &cap);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        cap = cudaStreamCaptureStatusActive;
-    }
-    const bool two_streams =
-        ctx->workspace_bytes >= nvfp4_linear_workspace_size() && cap == cudaStreamCaptureStatusNone;
+    // W's quantization (its own 8 KB of the larger workspace) beside X's
+    const bool two_streams = ctx->workspace_bytes >= nvfp4_linear_workspace_size();
     void* ws_w = static_cast<uint8_t*>(ctx->workspace) + (two_streams ? 2 * kSinglePassWorkspaceBytes : 0);
-    auto quantize_w = [&](cudaStream_t ws) {
-        return nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq, ws_w,
-                              kSinglePassWorkspaceBytes, reinterpret_cast<nvfp4_stream_t>(ws));
-    };
-    if (!two_streams) {
-        if ((st = linear_quantize_x(X, with_rht, rht_seed, ctx, stream)) || (st = quantize_w(s))) return st;
-    } else {
-        std::lock_guard<std::mutex> lk(g_side_mu);
-        SideStream* side;
-        if ((st = side_stream(&side))) return st;
-        e = cudaEventRecord(side->fork, s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "fork to the second stream: %s", cudaGetErrorString(e));
-        // whatever fails, the second stream is joined back before returning
-        st = quantize_w(side->stream);
-        if (!st) st = linear_quantize_x(X, with_rht, rht_seed, ctx, stream);
-        e = cudaEventRecord(side->join, side->stream);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join, 0);
-        if (st) return st;
-        if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "join of the second stream: %s", cudaGetErrorString(e));
-    }
+    if ((st = fork_join(
+             s, two_streams,
+             [&](cudaStream_t ws) {
+                 return nvfp4_quantize(W, NVFP4_IN_BF16, N, K, K, NVFP4_BLOCK_16x16, NVFP4_RTN, 0, &ctx->wq, &ctx->wtq,
+                                       ws_w, kSinglePassWorkspaceBytes, reinterpret_cast<nvfp4_stream_t>(ws));
+             },
+             [&]() { return linear_quantize_x(X, with_rht, rht_seed, ctx, stream); })))
+        return st;
     return nvfp4_gemm(&ctx->xq, &ctx->wq, Y, NVFP4_OUT_BF16, N, nullptr, 0, stream);
 }
 }  // namespace
