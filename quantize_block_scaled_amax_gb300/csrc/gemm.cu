@@ -22,7 +22,9 @@
 // 512 MMA cycles (about 74 B/cycle with scales).
 //
 // Pair tile 256 x 256, K staged 256 at a time (64 bf16 for the BF16 form);
-// one persistent cluster per SM pair.  Per CTA, 16 warps:
+// one persistent cluster per SM pair, working through one GEMM's tiles or
+// two GEMMs' (a layer's Dgrad and Wgrad, dealt so that the second fills the
+// SM pairs the first's last round leaves idle).  Per CTA, 16 warps:
 //   warp 0      code producer: its 128 A rows and its 128 B rows of the
 //               stage by TMA (128-byte swizzle), completing on the leader
 //               CTA's `full` barrier; 5-stage ring (38 KB per stage).
