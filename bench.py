@@ -827,6 +827,12 @@ def profile_case(args):
         dy = workloads.gradients(m, n, device=dev)
         torch.cuda.synchronize()
         nv.nvfp4_quantize(dy, round="sr", seed=workloads.SR_SEED)
+    elif op == "rht_x_rtn":
+        # the RHT colwise RTN quantization of an activation (the FFN down
+        # layer's input: 8192 x 20480 by default)
+        x = workloads.activations(m, n, device=dev)
+        torch.cuda.synchronize()
+        nv.nvfp4_rht_quantize(x, rht_seed=workloads.RHT_SEED)
     elif op == "rht_dy_sr":
         dy = workloads.gradients(m, n, device=dev)
         torch.cuda.synchronize()
@@ -856,7 +862,7 @@ def main():
     ap.add_argument("--cpu-sample-n", type=int, default=4096)
     ap.add_argument("--profile", default=None,
                     help="run one launch of one op: gemm_fprop, gemm, gemm_fp32, gemm_pair, quant_x_rtn, quant_w_2d, "
-                         "quant_dy_sr, rht_dy_sr")
+                         "quant_dy_sr, rht_dy_sr, rht_x_rtn")
     ap.add_argument("--m", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)
     ap.add_argument("--k", type=int, default=0)
