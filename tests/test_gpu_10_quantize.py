@@ -150,6 +150,27 @@ def test_rht_colwise(nv, shape, dtype, rounding):
                        what="rht colwise")
 
 
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("rht", [False, True])
+def test_colwise_several_tiles_per_cta(nv, rounding, rht):
+    # 4240 x 4176: 34 x 66 = 2244 tiles of 128 x 64, more than the grid (at
+    # most 12 CTAs per SM), so CTAs walk several tiles and the bf16 kernel's
+    # double buffer (the next tile copied while one is encoded) turns over;
+    # the last tile row and column are partial.  Checked whole against the
+    # oracle.
+    x = workloads.normal_with_outliers(4240, 4176, p=0.001, factor=20.0, seed=4241, dtype=torch.bfloat16)
+    xn = to_f32_np(x)
+    if rht:
+        q = nv.nvfp4_rht_quantize(x.cuda(), round=rounding, seed=91, rht_seed=workloads.RHT_SEED)
+        ref = oracle.quantize(xn, layout="col", rounding=rounding, seed=91, rht_seed=workloads.RHT_SEED)
+    else:
+        _, q = nv.nvfp4_quantize(x.cuda(), round=rounding, seed=91, rowwise=False, colwise=True)
+        ref = oracle.quantize(xn, layout="col", rounding=rounding, seed=91)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_sync_status() == nv.OK
+    assert_quant_equal(q, ref, what="colwise, several tiles per CTA")
+
+
 # ---- edge cases ----------------------------------------------------------------
 
 def test_all_zero_tensor(nv):
