@@ -249,6 +249,12 @@ def test_linear_argument_checks_need_no_gpu(L):
     assert fwd(ctx(wq=t(N, K, layout=0))) == q.ERR_INVALID_ARG                        # wq needs MMA scales
     assert fwd(ctx(wtq=t(N, K))) == q.ERR_INVALID_ARG                                 # wtq is [K][N]
     assert b"wtq" in L.nvfp4_last_error()
+    assert fwd(ctx(workspace_bytes=8192)) == q.ERR_WORKSPACE                          # below 16 KB
+    # a W that its own quantization refuses (not 16-byte aligned): the error
+    # comes back through the forward's fork/join, whichever stream W was on
+    lw = q.nvfp4_linear_workspace_size()
+    assert L.nvfp4_linear_fwd(16, 24, 16, ctypes.byref(ctx(workspace_bytes=lw)), None) == q.ERR_INVALID_ARG
+    assert b"aligned" in L.nvfp4_last_error()
 
     # the forward that also writes Wgrad's X^T codes checks xtq as well
     fwd_rht = lambda c, x=16: L.nvfp4_linear_fwd_rht(x, 16, 16, 5, ctypes.byref(c) if c is not None else None, None)
